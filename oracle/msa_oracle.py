@@ -1,0 +1,305 @@
+"""Plain fp64 CPU oracle for MiniMax Sparse Attention (MSA).
+
+TEST INFRASTRUCTURE ONLY.  This module is the independent reference the CUDA
+library is checked against.  Only the test suite, the package smoke check and the
+benchmark's CPU-baseline leg may import it; the library itself never does, and this
+module imports nothing from the library.
+
+What it follows (cited by page title and section):
+
+* "Sparse Attention Cannot Be Directly Ported Across Architectures" (disconfirmai.com
+  news article), paragraph introducing MSA: a lightweight index branch runs full
+  attention with four query heads and one key head; the main branch attends only to
+  the blocks the index selects.  Paragraph "MSA addresses these issues": the index
+  outputs are not aggregated, each KV head selects its own set, and retrieval is per
+  block rather than per token.
+* "How MiniMax M3 was built" (aietalks.com), sections "MSA uses a lightweight index
+  branch before sparse attention" and "Block-level retrieval makes sparse attention
+  easier to run on GPUs" -- the same two branches and the per-head block retrieval.
+* The Chinese topic page on MSA (disconfirmai.com), summary paragraph: each KV head
+  independently selects its top-k key/value blocks and the main branch computes exact
+  attention only on the selected blocks.
+
+The pages fix no block size, k, pooling rule, scale or tie-break.  The readings
+taken here are: index logits scaled by index_scale (1/sqrt(dI) by default) and
+pooled raw (no softmax / ReLU / head weights); a block's score for a query tile is
+the MAX over the tile's queries and the block's keys of the causally visible logits;
+k counts the current block, which is always kept; the other k-1 blocks are the
+highest scores, ties to the lower block index, compared as reals (-0 == +0); the
+result is written ascending and padded with -1; fewer than k visible blocks means
+all of them are taken.  Attention is exact softmax over the union of the selected
+blocks intersected with the causal range, with all G query heads of a KV group
+sharing their group's selection (head h uses KV head h // G).
+
+Everything is computed in float64.  Inputs stored as bf16 or fp32 are exactly
+representable in float64, so the oracle sees the very values the kernels see.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(x) -> np.ndarray:
+    """Any array-like (numpy or torch, any float dtype) as a float64 numpy array."""
+    if hasattr(x, "detach"):                      # torch tensor: go through fp32
+        x = x.detach().to("cpu").float().numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def default_scale(dim: int) -> float:
+    """Softmax scale used when a caller passes 0: 1/sqrt(dim)."""
+    return 1.0 / np.sqrt(dim)
+
+
+# ---------------------------------------------------------------------------
+# Index branch: causal index logits, max-pooled per (query tile, key block)
+# ---------------------------------------------------------------------------
+
+def index_logits(idx_q_rows, idx_k, index_scale, q_pos):
+    """Causal index logits for a set of query tokens.
+
+    idx_q_rows [n, NI, dI] are the index queries of n tokens at positions q_pos[n];
+    idx_k [L, dI] is the single shared index key head.  Returns s [NI, n, L] with
+    s[g, i, j] = index_scale * <idx_q_rows[i, g], idx_k[j]> for j <= q_pos[i] and -inf
+    for j > q_pos[i] (four index query heads against one key head: the MSA paragraph of
+    the disconfirmai.com article).
+    """
+    qr = _f64(idx_q_rows)
+    kk = _f64(idx_k)
+    s = index_scale * np.einsum("ngc,jc->gnj", qr, kk)
+    j = np.arange(kk.shape[0])
+    visible = j[None, :] <= np.asarray(q_pos)[:, None]          # [n, L]
+    return np.where(visible[None, :, :], s, -np.inf)
+
+
+def pool_blocks(s, block_size):
+    """Max of s [NI, n, L] over all n query rows and over each key block of block_size.
+
+    Returns [NI, nB]; a block with no visible key gives -inf.  Block-level retrieval:
+    "Block-level retrieval makes sparse attention easier to run on GPUs" (aietalks.com).
+    """
+    NI, n, L = s.shape
+    nB = -(-L // block_size)
+    pad = nB * block_size - L
+    if pad:
+        s = np.concatenate([s, np.full((NI, n, pad), -np.inf)], axis=2)
+    return s.reshape(NI, n, nB, block_size).max(axis=(1, 3))
+
+
+def index_block_scores_prefill(idx_q, idx_k, block_size, q_tile, index_scale=None,
+                               tiles=None):
+    """Prefill block scores S[b, g, m, blk] for query tiles m of q_tile tokens.
+
+    idx_q [B, T, NI, dI], idx_k [B, T, dI].  Tile m holds tokens m*q_tile .. (m+1)*q_tile-1
+    (the last tile may be short).  S is the max, over the tile's tokens t and the block's
+    keys j <= t, of the scaled index logit; -inf when no key of the block is visible.
+    ``tiles`` restricts the result to a list of tile indices (axis 2 follows that list).
+    """
+    qi, ki = _f64(idx_q), _f64(idx_k)
+    B, T, NI, dI = qi.shape
+    if index_scale is None or index_scale == 0:
+        index_scale = default_scale(dI)
+    nT = -(-T // q_tile)
+    tile_list = list(range(nT)) if tiles is None else [int(m) for m in tiles]
+    nB = -(-T // block_size)
+    out = np.empty((B, NI, len(tile_list), nB))
+    for b in range(B):
+        for col, m in enumerate(tile_list):
+            t = np.arange(m * q_tile, min(T, (m + 1) * q_tile))
+            s = index_logits(qi[b, t], ki[b], index_scale, t)
+            out[b, :, col, :] = pool_blocks(s, block_size)
+    return out
+
+
+def index_block_scores_decode(idx_q, idx_k, block_size, index_scale=None):
+    """Decode block scores S[b, g, 0, blk] for the one new token at position L-1.
+
+    idx_q [B, 1, NI, dI] (the new token's index queries), idx_k [B, L, dI] (the index-key
+    cache, the new token included).  Selection is per token in decode.
+    """
+    qi, ki = _f64(idx_q), _f64(idx_k)
+    B, _, NI, dI = qi.shape
+    L = ki.shape[1]
+    if index_scale is None or index_scale == 0:
+        index_scale = default_scale(dI)
+    nB = -(-L // block_size)
+    out = np.empty((B, NI, 1, nB))
+    for b in range(B):
+        s = index_logits(qi[b, 0:1], ki[b], index_scale, np.array([L - 1]))
+        out[b, :, 0, :] = pool_blocks(s, block_size)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Per-KV-head block top-k
+# ---------------------------------------------------------------------------
+
+def current_block(last_query_pos: int, block_size: int) -> int:
+    """The block that holds a tile's last query: it is always selected."""
+    return int(last_query_pos) // block_size
+
+
+def select_blocks(row_scores, cur: int, top_k: int):
+    """One row of the per-KV-head selection.
+
+    Candidates are blocks 0..cur (no block after the current one holds a visible key).
+    The current block is kept; the other top_k-1 are the best of 0..cur-1 by score,
+    descending, ties to the lower block index, scores compared as reals so that -0 and
+    +0 tie.  Returned ascending, padded with -1 to top_k entries.  (Independent top-k per
+    KV head: the Chinese topic page's summary; "MSA addresses these issues" paragraph of
+    the disconfirmai.com article.)
+    """
+    r = np.asarray(row_scores, dtype=np.float64)[:cur]
+    idx = np.arange(cur)
+    order = np.lexsort((idx, -r))             # primary key -score, then block index
+    chosen = np.sort(np.concatenate([order[: top_k - 1], [cur]]))
+    out = np.full(top_k, -1, dtype=np.int32)
+    out[: len(chosen)] = chosen
+    return out
+
+
+def block_topk_prefill(scores, seq_len, q_tile, block_size, top_k, tiles=None):
+    """sel[b, g, m, :] for prefill block scores [B, NI, nT (or len(tiles)), nB]."""
+    sc = np.asarray(scores, dtype=np.float64)
+    B, NI, nR, _ = sc.shape
+    nT = -(-seq_len // q_tile)
+    tile_list = list(range(nT)) if tiles is None else [int(m) for m in tiles]
+    assert len(tile_list) == nR
+    sel = np.empty((B, NI, nR, top_k), dtype=np.int32)
+    for col, m in enumerate(tile_list):
+        cur = current_block(min(seq_len - 1, m * q_tile + q_tile - 1), block_size)
+        for b in range(B):
+            for g in range(NI):
+                sel[b, g, col] = select_blocks(sc[b, g, col], cur, top_k)
+    return sel
+
+
+def block_topk_decode(scores, seq_len, block_size, top_k):
+    """sel[b, g, 0, :] for decode block scores [B, NI, 1, nB]; the query is at seq_len-1."""
+    sc = np.asarray(scores, dtype=np.float64)
+    B, NI, _, _ = sc.shape
+    cur = current_block(seq_len - 1, block_size)
+    sel = np.empty((B, NI, 1, top_k), dtype=np.int32)
+    for b in range(B):
+        for g in range(NI):
+            sel[b, g, 0] = select_blocks(sc[b, g, 0], cur, top_k)
+    return sel
+
+
+# ---------------------------------------------------------------------------
+# Main branch: exact softmax attention over the selected blocks
+# ---------------------------------------------------------------------------
+
+def selected_keys(sel_row, block_size, seq_k):
+    """All key positions of the selected blocks of one row (padding -1 ignored)."""
+    blocks = [int(b) for b in sel_row if b >= 0]
+    if not blocks:
+        return np.zeros(0, dtype=np.int64)
+    return np.concatenate([np.arange(b * block_size, min(seq_k, (b + 1) * block_size))
+                           for b in blocks])
+
+
+def sparse_attention(q, k, v, sel, block_size, q_tile, sm_scale=None, q_offset=0,
+                     tiles=None):
+    """Exact attention of every query head over its KV group's selected blocks.
+
+    q [B, Sq, Hq, d] with query i at position q_offset + i; k, v [B, Hkv, Sk, d];
+    sel [B, Hkv, nT, top_k] (one row per tile of q_tile queries).  For query t and head
+    h (KV head g = h // G): J = keys of the selected blocks with j <= t,
+    z_j = sm_scale * <q[t, h], k[g, j]>, lse = log sum_J exp(z_j),
+    out = sum_J exp(z_j - lse) v[g, j].  A row with empty J gets out = 0, lse = -inf.
+    The main branch "attends only to the selected blocks" (aietalks.com, section "MSA
+    uses a lightweight index branch before sparse attention"), exactly (Chinese topic
+    page summary), with the GQA group sharing its KV head's selection.
+
+    Returns (out [B, Sq, Hq, d] or only the listed tiles' rows, lse [B, Hq, Sq or rows]).
+    """
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    B, Sq, Hq, d = qf.shape
+    Hkv, Sk = kf.shape[1], kf.shape[2]
+    G = Hq // Hkv
+    if sm_scale is None or sm_scale == 0:
+        sm_scale = default_scale(d)
+    nT = -(-Sq // q_tile)
+    tile_list = list(range(nT)) if tiles is None else [int(m) for m in tiles]
+    rows = np.concatenate([np.arange(m * q_tile, min(Sq, (m + 1) * q_tile))
+                           for m in tile_list]) if tile_list else np.zeros(0, int)
+    out = np.zeros((B, len(rows), Hq, d))
+    lse = np.full((B, Hq, len(rows)), -np.inf)
+    r0 = 0
+    for m in tile_list:
+        t_idx = np.arange(m * q_tile, min(Sq, (m + 1) * q_tile))
+        pos = q_offset + t_idx
+        for b in range(B):
+            for g in range(Hkv):
+                J = selected_keys(sel[b, g, m], block_size, Sk)
+                if J.size == 0:
+                    continue
+                heads = np.arange(g * G, (g + 1) * G)
+                z = sm_scale * np.einsum("thc,jc->thj", qf[b][np.ix_(t_idx, heads)],
+                                         kf[b, g, J])
+                z = np.where((J[None, None, :] <= pos[:, None, None]), z, -np.inf)
+                zmax = z.max(axis=2, keepdims=True)
+                has = np.isfinite(zmax[..., 0])
+                zmax = np.where(np.isfinite(zmax), zmax, 0.0)
+                e = np.exp(z - zmax)
+                ssum = e.sum(axis=2)
+                with np.errstate(divide="ignore", invalid="ignore"):
+                    l = np.where(has, np.log(ssum) + zmax[..., 0], -np.inf)
+                    p = np.where(has[..., None], e / ssum[..., None], 0.0)
+                o = np.einsum("thj,jc->thc", p, vf[b, g, J])
+                out[b, r0:r0 + len(t_idx), g * G:(g + 1) * G, :] = o
+                lse[b, g * G:(g + 1) * G, r0:r0 + len(t_idx)] = l.T
+        r0 += len(t_idx)
+    return out, lse
+
+
+def full_causal_gqa(q, k, v, sm_scale=None, q_offset=0):
+    """Dense causal GQA attention (every key j <= t), the k = all-blocks limit of MSA."""
+    qf, kf, vf = _f64(q), _f64(k), _f64(v)
+    B, Sq, Hq, d = qf.shape
+    Hkv, Sk = kf.shape[1], kf.shape[2]
+    G = Hq // Hkv
+    if sm_scale is None or sm_scale == 0:
+        sm_scale = default_scale(d)
+    kh = np.repeat(kf, G, axis=1)                       # [B, Hq, Sk, d]
+    vh = np.repeat(vf, G, axis=1)
+    z = sm_scale * np.einsum("bthc,bhjc->bhtj", qf, kh)
+    pos = q_offset + np.arange(Sq)
+    z = np.where(np.arange(Sk)[None, None, None, :] <= pos[None, None, :, None], z, -np.inf)
+    zmax = z.max(axis=3, keepdims=True)
+    e = np.exp(z - zmax)
+    ssum = e.sum(axis=3, keepdims=True)
+    lse = (np.log(ssum) + zmax)[..., 0]                # [B, Hq, Sq]
+    out = np.einsum("bhtj,bhjc->bthc", e / ssum, vh)
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# Whole pipelines (index -> top-k -> attention), as the three stages chain
+# ---------------------------------------------------------------------------
+
+def msa_prefill(q, k, v, idx_q, idx_k, block_size, q_tile, top_k, sm_scale=None,
+                index_scale=None, tiles=None):
+    """Index scores, per-KV-head selection and sparse attention for prefill."""
+    T = q.shape[1]
+    scores = index_block_scores_prefill(idx_q, idx_k, block_size, q_tile, index_scale, tiles)
+    sel = block_topk_prefill(scores, T, q_tile, block_size, top_k, tiles)
+    nT = -(-T // q_tile)
+    if tiles is None:
+        full_sel = sel
+    else:
+        full_sel = np.full(sel.shape[:2] + (nT, top_k), -1, dtype=np.int32)
+        full_sel[:, :, [int(m) for m in tiles]] = sel
+    out, lse = sparse_attention(q, k, v, full_sel, block_size, q_tile, sm_scale, 0, tiles)
+    return scores, sel, out, lse
+
+
+def msa_decode(q, k_cache, v_cache, idx_q, idx_k, block_size, top_k, sm_scale=None,
+               index_scale=None):
+    """One decode step: the new token (position L-1) scores, selects and attends."""
+    L = k_cache.shape[2]
+    scores = index_block_scores_decode(idx_q, idx_k, block_size, index_scale)
+    sel = block_topk_decode(scores, L, block_size, top_k)
+    out, lse = sparse_attention(q, k_cache, v_cache, sel, block_size, 1, sm_scale, L - 1)
+    return scores, sel, out, lse

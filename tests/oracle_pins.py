@@ -1,0 +1,397 @@
+"""Pins for the fp64 oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` takes the oracle module (or a deliberately broken copy of it, see
+test_oracle_mutations.py) and raises AssertionError when the module disagrees with
+
+* a library routine (numpy matmul, torch scaled_dot_product_attention in fp64),
+* brute force written as plain Python loops on tiny inputs,
+* exhaustive enumeration of the top-k subsets,
+* closed forms and invariants of the definition (rows sum to one, unselected K/V do
+  not matter, k = all blocks is full causal attention, decode = last prefill row),
+* a case worked by hand (tests/golden/worked_example_t6.json),
+* the planted-block and head-diversity properties of the seeded inputs.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# ----------------------------------------------------------------- index branch
+
+def pin_scores_block1_tile1(o):
+    """block = tile = 1: the block scores are the masked index logits (numpy matmul)."""
+    r = _rng(1)
+    B, T, NI, dI = 2, 9, 4, 5
+    q, k = r.standard_normal((B, T, NI, dI)), r.standard_normal((B, T, dI))
+    scale = 0.37
+    got = o.index_block_scores_prefill(q, k, 1, 1, scale)
+    for b in range(B):
+        for g in range(NI):
+            ref = scale * np.matmul(q[b, :, g, :], k[b].T)           # [T, T]
+            ref[np.triu_indices(T, 1)] = -np.inf
+            assert np.array_equal(np.isinf(got[b, g]), np.isinf(ref))
+            fin = np.isfinite(ref)
+            assert np.allclose(got[b, g][fin], ref[fin], rtol=1e-13, atol=1e-13)
+
+
+def _brute_scores(q, k, bs, qt, scale, positions_of_tile):
+    """Plain loops: max over tile rows t, block keys j <= t, of scale * sum_c q*k."""
+    B, _, NI, dI = len(q), None, len(q[0][0]), len(q[0][0][0])
+    L = len(k[0])
+    nB = -(-L // bs)
+    out = []
+    for b in range(B):
+        per_g = []
+        for g in range(NI):
+            rows = []
+            for (rows_t, pos_t) in positions_of_tile:
+                row = []
+                for blk in range(nB):
+                    best = -math.inf
+                    for qi, t in zip(rows_t, pos_t):
+                        for j in range(blk * bs, min(L, blk * bs + bs)):
+                            if j > t:
+                                continue
+                            s = 0.0
+                            for c in range(dI):
+                                s += q[b][qi][g][c] * k[b][j][c]
+                            best = max(best, scale * s)
+                    row.append(best)
+                rows.append(row)
+            per_g.append(rows)
+        out.append(per_g)
+    return np.array(out)
+
+
+def pin_scores_bruteforce(o):
+    """Ragged T, block 4, tile 2: the pooled scores equal triple loops."""
+    r = _rng(2)
+    B, T, NI, dI, bs, qt = 1, 11, 2, 3, 4, 2
+    q, k = r.standard_normal((B, T, NI, dI)), r.standard_normal((B, T, dI))
+    tiles = [(list(range(m * qt, min(T, m * qt + qt))),) * 2 for m in range(-(-T // qt))]
+    ref = _brute_scores(q.tolist(), k.tolist(), bs, qt, 0.5, tiles)
+    got = o.index_block_scores_prefill(q, k, bs, qt, 0.5)
+    assert got.shape == ref.shape
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+    fin = np.isfinite(ref)
+    assert np.allclose(got[fin], ref[fin], rtol=1e-12, atol=1e-12)
+
+
+def pin_decode_scores_bruteforce(o):
+    """Decode: one query at position L-1 against the whole cache, ragged last block."""
+    r = _rng(3)
+    B, L, NI, dI, bs = 2, 13, 4, 3, 4
+    q, k = r.standard_normal((B, 1, NI, dI)), r.standard_normal((B, L, dI))
+    ref = _brute_scores(q.tolist(), k.tolist(), bs, 1, 0.25, [([0], [L - 1])])
+    got = o.index_block_scores_decode(q, k, bs, 0.25)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------- top-k
+
+def _dominates(scores, chosen, cur):
+    """Every chosen non-current block beats every unchosen candidate (desc score, asc idx)."""
+    others = [b for b in range(cur) if b not in chosen]
+    for a in chosen:
+        if a == cur:
+            continue
+        for b in others:
+            if not (scores[a] > scores[b] or (scores[a] == scores[b] and a < b)):
+                return False
+    return True
+
+
+def pin_topk_bruteforce(o):
+    """Enumerate every k-subset holding the current block: exactly one dominates."""
+    r = _rng(4)
+    for trial in range(300):
+        cur = int(r.integers(0, 11))
+        top_k = int(r.integers(1, 5))
+        # small integers make ties common; signed zeros must tie with each other
+        vals = r.integers(-2, 3, size=cur + 1).astype(np.float64)
+        zeros = vals == 0
+        vals[zeros] = np.where(r.random(zeros.sum()) < 0.5, 0.0, -0.0)
+        if trial % 7 == 0:
+            vals = r.standard_normal(cur + 1)
+        row = np.concatenate([vals, np.full(3, -np.inf)])
+        got = o.select_blocks(row, cur, top_k)
+        want_n = min(top_k, cur + 1)
+        winners = []
+        for sub in itertools.combinations(range(cur), want_n - 1):
+            chosen = sorted(set(sub) | {cur})
+            if _dominates(list(vals), chosen, cur):
+                winners.append(chosen)
+        assert len(winners) == 1, (vals, top_k, winners)
+        expect = np.full(top_k, -1)
+        expect[:want_n] = winners[0]
+        assert np.array_equal(got, expect), (vals, cur, top_k, got, expect)
+
+
+def pin_topk_layout(o):
+    """Prefill/decode wrappers: the current block comes from the tile's last query."""
+    T, qt, bs, k = 21, 4, 8, 3
+    nT, nB = -(-T // qt), -(-T // bs)
+    scores = np.arange(nB, dtype=np.float64)[None, None, None, :].repeat(nT, axis=2)
+    sel = o.block_topk_prefill(scores, T, qt, bs, k)
+    for m in range(nT):
+        last = min(T - 1, m * qt + qt - 1)
+        cur = last // bs
+        want = sorted(set(range(max(0, cur - (k - 1)), cur)) | {cur})   # increasing scores
+        expect = np.full(k, -1)
+        expect[:len(want)] = want
+        assert np.array_equal(sel[0, 0, m], expect), (m, sel[0, 0, m], expect)
+    dsel = o.block_topk_decode(scores[:, :, :1], T, bs, k)
+    assert np.array_equal(dsel[0, 0, 0], [0, 1, 2])                     # cur = 20 // 8 = 2
+    # a query that opens a block: position 16 with block 8 has current block 2
+    dsel = o.block_topk_decode(scores[:, :, :1], 17, bs, 2)
+    assert np.array_equal(dsel[0, 0, 0], [1, 2]), dsel[0, 0, 0]
+    psel = o.block_topk_prefill(np.zeros((1, 1, 17, 3)), 17, 1, bs, 1)
+    assert [int(psel[0, 0, t, 0]) for t in (7, 8, 15, 16)] == [0, 1, 1, 2]
+
+
+# ------------------------------------------------------------------- attention
+
+def _brute_attention(q, k, v, sel, bs, qt, scale, q_offset):
+    """Plain loops over (b, t, h): softmax over selected, causally visible keys."""
+    B, Sq, Hq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((B, Sq, Hq, d))
+    lse = np.full((B, Hq, Sq), -np.inf)
+    for b in range(B):
+        for t in range(Sq):
+            pos = q_offset + t
+            for h in range(Hq):
+                g = h // G
+                keys = []
+                for blk in sel[b, g, t // qt]:
+                    if blk < 0:
+                        continue
+                    for j in range(blk * bs, min(Sk, blk * bs + bs)):
+                        if j <= pos:
+                            keys.append(j)
+                if not keys:
+                    continue
+                z = [scale * sum(q[b, t, h, c] * k[b, g, j, c] for c in range(d)) for j in keys]
+                zm = max(z)
+                w = [math.exp(x - zm) for x in z]
+                s = sum(w)
+                lse[b, h, t] = zm + math.log(s)
+                for c in range(d):
+                    out[b, t, h, c] = sum(wi * v[b, g, j, c] for wi, j in zip(w, keys)) / s
+    return out, lse
+
+
+def _small_attn_case(seed, B=1, T=10, Hq=4, Hkv=2, d=3):
+    r = _rng(seed)
+    return (r.standard_normal((B, T, Hq, d)), r.standard_normal((B, Hkv, T, d)),
+            r.standard_normal((B, Hkv, T, d)))
+
+
+def pin_full_k_bruteforce(o):
+    """k >= number of blocks: MSA is full causal GQA attention (plain loops)."""
+    q, k, v = _small_attn_case(5)
+    T, bs, qt = 10, 4, 2
+    nT, nB = -(-T // qt), -(-T // bs)
+    sel = o.block_topk_prefill(np.zeros((1, 2, nT, nB)), T, qt, bs, nB + 1)
+    out, lse = o.sparse_attention(q, k, v, sel, bs, qt, 0.7)
+    ref_o, ref_l = _brute_attention(q, k, v, sel, bs, qt, 0.7, 0)
+    assert np.allclose(out, ref_o, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse, ref_l, rtol=1e-12, atol=1e-12)
+    fo, fl = o.full_causal_gqa(q, k, v, 0.7)
+    assert np.allclose(fo, ref_o, rtol=1e-12, atol=1e-12)
+    assert np.allclose(fl, ref_l, rtol=1e-12, atol=1e-12)
+
+
+def pin_full_k_sdpa(o):
+    """k = all blocks against torch's scaled_dot_product_attention in float64."""
+    import torch
+    r = _rng(6)
+    B, T, Hq, Hkv, d, bs, qt = 2, 70, 8, 4, 16, 16, 8
+    q = r.standard_normal((B, T, Hq, d))
+    k = r.standard_normal((B, Hkv, T, d))
+    v = r.standard_normal((B, Hkv, T, d))
+    nT, nB = -(-T // qt), -(-T // bs)
+    sel = o.block_topk_prefill(r.standard_normal((B, Hkv, nT, nB)), T, qt, bs, nB)
+    out, lse = o.sparse_attention(q, k, v, sel, bs, qt, None)
+    tq = torch.from_numpy(q).permute(0, 2, 1, 3)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        tq, torch.from_numpy(k), torch.from_numpy(v), is_causal=True, enable_gqa=True)
+    assert np.allclose(out, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-10)
+    kk = torch.from_numpy(k).repeat_interleave(Hq // Hkv, dim=1)
+    z = (tq @ kk.transpose(-1, -2)) / math.sqrt(d)
+    z = z.masked_fill(torch.triu(torch.ones(T, T, dtype=torch.bool), 1), -math.inf)
+    assert np.allclose(lse, torch.logsumexp(z, dim=-1).numpy(), rtol=1e-10, atol=1e-10)
+
+
+def _random_sel(o, T, qt, bs, k, Hkv, seed, B=1):
+    r = _rng(seed)
+    nT, nB = -(-T // qt), -(-T // bs)
+    return o.block_topk_prefill(r.standard_normal((B, Hkv, nT, nB)), T, qt, bs, k)
+
+
+def pin_sparse_bruteforce(o):
+    """A sparse selection: output and lse equal the plain-loop restatement."""
+    q, k, v = _small_attn_case(7, B=2, T=23, Hq=6, Hkv=3, d=4)
+    T, bs, qt, kk = 23, 4, 2, 3
+    sel = _random_sel(o, T, qt, bs, kk, 3, 8, B=2)
+    out, lse = o.sparse_attention(q, k, v, sel, bs, qt, 0.6)
+    ref_o, ref_l = _brute_attention(q, k, v, sel, bs, qt, 0.6, 0)
+    assert np.allclose(out, ref_o, rtol=1e-12, atol=1e-12)
+    assert np.allclose(lse, ref_l, rtol=1e-12, atol=1e-12)
+
+
+def pin_rows_sum_to_one(o):
+    """With V = 1 every output is 1 (the weights sum to one), for any selection."""
+    q, k, _ = _small_attn_case(9, T=40, Hq=4, Hkv=2, d=5)
+    v = np.ones_like(k)
+    sel = _random_sel(o, 40, 4, 8, 2, 2, 10)
+    out, lse = o.sparse_attention(q, k, v, sel, 8, 4, None)
+    assert np.allclose(out, 1.0, rtol=0, atol=1e-13)
+    assert np.all(np.isfinite(lse))
+
+
+def pin_unselected_invariance(o):
+    """Changing K/V inside blocks no tile selects leaves the output unchanged."""
+    q, k, v = _small_attn_case(11, T=48, Hq=4, Hkv=2, d=4)
+    T, bs, qt = 48, 8, 4
+    nT, nB = T // qt, T // bs
+    sel = np.full((1, 2, nT, 2), -1, dtype=np.int32)
+    for m in range(nT):
+        cur = (m * qt + qt - 1) // bs
+        sel[0, :, m, 0] = 0 if cur > 0 else -1
+        sel[0, :, m, 1] = cur
+        if cur == 0:
+            sel[0, :, m] = [0, -1]
+    out1, lse1 = o.sparse_attention(q, k, v, sel, bs, qt, None)
+    k2, v2 = k.copy(), v.copy()
+    # blocks 1..nB-1 are only ever used as the current block, so block 1's keys are
+    # unseen by tiles of blocks 2+; change them where only those tiles could look
+    r = _rng(12)
+    for g in range(2):
+        for j in range(bs, 2 * bs):
+            k2[0, g, j] = r.standard_normal(4) * 5
+            v2[0, g, j] = r.standard_normal(4) * 5
+    out2, lse2 = o.sparse_attention(q, k2, v2, sel, bs, qt, None)
+    rows = np.arange(2 * bs, T)              # queries whose tiles do not select block 1
+    assert np.allclose(out1[0, rows], out2[0, rows], rtol=0, atol=0)
+    assert np.allclose(lse1[0][:, rows], lse2[0][:, rows], rtol=0, atol=0)
+    changed = np.arange(bs, 2 * bs)          # queries inside block 1 must see the change
+    assert not np.allclose(out1[0, changed], out2[0, changed])
+
+
+def pin_decode_equals_prefill_row(o):
+    """Decode at cache length L = the prefill row t = L-1 with q_tile = 1."""
+    r = _rng(13)
+    B, L, Hq, Hkv, d, dI, bs, kk = 1, 37, 8, 4, 6, 5, 8, 3
+    q = r.standard_normal((B, L, Hq, d))
+    k = r.standard_normal((B, Hkv, L, d))
+    v = r.standard_normal((B, Hkv, L, d))
+    iq = r.standard_normal((B, L, Hkv, dI))
+    ik = r.standard_normal((B, L, dI))
+    sc_p, sel_p, out_p, lse_p = o.msa_prefill(q, k, v, iq, ik, bs, 1, kk)
+    sc_d, sel_d, out_d, lse_d = o.msa_decode(q[:, L - 1:], k, v, iq[:, L - 1:], ik, bs, kk)
+    assert np.array_equal(sc_d[:, :, 0], sc_p[:, :, L - 1])
+    assert np.array_equal(sel_d[:, :, 0], sel_p[:, :, L - 1])
+    assert np.allclose(out_d[:, 0], out_p[:, L - 1], rtol=1e-13, atol=1e-13)
+    assert np.allclose(lse_d[:, :, 0], lse_p[:, :, L - 1], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------ seeded-input properties
+
+def _tiny_scaled_inputs():
+    from block_sparse_gqa_02_gb300.configs import CONFIGS
+    from block_sparse_gqa_02_gb300.inputs import make_inputs
+    cfg = CONFIGS["tiny"]
+    return cfg, make_inputs(cfg, input_scale=cfg.head_dim ** -0.5, plant_alpha=3.0)
+
+
+def pin_planted_selected(o):
+    """Scaled tiny inputs: every planted block before a tile's current block is chosen."""
+    cfg, x = _tiny_scaled_inputs()
+    sc = o.index_block_scores_prefill(x["idx_q"], x["idx_k"], cfg.block_size, cfg.q_tile)
+    sel = o.block_topk_prefill(sc, cfg.seq, cfg.q_tile, cfg.block_size, cfg.top_k)
+    hits = 0
+    for g in range(cfg.n_heads_kv):
+        for m in range(cfg.n_tiles):
+            cur = (m * cfg.q_tile + cfg.q_tile - 1) // cfg.block_size
+            before = [int(p) for p in x["plants"][0, g] if p < cur]
+            for p in before:
+                assert p in sel[0, g, m], (g, m, p, sel[0, g, m])
+                hits += 1
+    assert hits > 0
+
+
+def pin_head_diversity(o):
+    """Different KV heads select different blocks (an aggregated selection would not)."""
+    cfg, x = _tiny_scaled_inputs()
+    sc = o.index_block_scores_prefill(x["idx_q"], x["idx_k"], cfg.block_size, cfg.q_tile)
+    sel = o.block_topk_prefill(sc, cfg.seq, cfg.q_tile, cfg.block_size, cfg.top_k)
+    differing = 0
+    for m in range(cfg.n_tiles):
+        rows = {tuple(sel[0, g, m]) for g in range(cfg.n_heads_kv)}
+        differing += len(rows) > 1
+    assert differing >= cfg.n_tiles // 2, differing
+
+
+# --------------------------------------------------------------- worked example
+
+def _val(x):
+    if isinstance(x, (int, float)):
+        return float(x)
+    if x == "-inf":
+        return -math.inf
+    if x.startswith("ln"):
+        return math.log(float(x[2:]))
+    if "/" in x:
+        a, b = x.split("/")
+        return float(a) / float(b)
+    return float(x)
+
+
+def pin_worked_example(o):
+    """The hand-worked T=6 case (tests/golden/worked_example_t6.json)."""
+    with open(os.path.join(GOLDEN, "worked_example_t6.json")) as f:
+        case = json.load(f)
+    inp, exp = case["inputs"], case["expected"]
+    sh = case["shape"]
+    T = sh["T"]
+    vec = lambda key: np.array([_val(x) for x in inp[key]])
+    idx_q = np.stack([vec("idx_q_head0"), vec("idx_q_head1")], axis=1)[None, :, :, None]
+    idx_k = vec("idx_k")[None, :, None]
+    q = np.stack([vec("q_head0"), vec("q_head1")], axis=1)[None, :, :, None]
+    k = np.stack([vec("k_head0"), vec("k_head1")], axis=0)[None, :, :, None]
+    v = np.stack([vec("v_head0"), vec("v_head1")], axis=0)[None, :, :, None]
+    sc, sel, out, lse = o.msa_prefill(q, k, v, idx_q, idx_k, sh["block_size"], sh["q_tile"],
+                                      sh["top_k"], sh["sm_scale"], sh["index_scale"])
+    for g in range(2):
+        want_sc = np.array([[_val(x) for x in row] for row in exp[f"scores_head{g}"]])
+        assert np.array_equal(np.isinf(sc[0, g]), np.isinf(want_sc))
+        assert np.allclose(sc[0, g][np.isfinite(want_sc)], want_sc[np.isfinite(want_sc)],
+                           atol=1e-15)
+        assert np.array_equal(sel[0, g], np.array(exp[f"sel_head{g}"])), (g, sel[0, g])
+        want_o = np.array([_val(x) for x in exp[f"out_head{g}"]])
+        want_l = np.array([_val(x) for x in exp[f"lse_head{g}"]])
+        assert np.allclose(out[0, :, g, 0], want_o, rtol=1e-13, atol=1e-13), out[0, :, g, 0]
+        assert np.allclose(lse[0, g], want_l, rtol=1e-13, atol=1e-13), lse[0, g]
+    assert out.shape == (1, T, 2, 1)
+
+
+ALL_PINS = [
+    pin_scores_block1_tile1, pin_scores_bruteforce, pin_decode_scores_bruteforce,
+    pin_topk_bruteforce, pin_topk_layout, pin_full_k_bruteforce, pin_full_k_sdpa,
+    pin_sparse_bruteforce, pin_rows_sum_to_one, pin_unselected_invariance,
+    pin_decode_equals_prefill_row, pin_planted_selected, pin_head_diversity,
+    pin_worked_example,
+]
