@@ -1,0 +1,416 @@
+"""Benchmark of the MSA hot path on one GB300 (or N independent replicas under torchrun).
+
+One step = one pass of the whole path:
+  * prefill at 128K context (index block scores -> per-KV-head top-k -> sparse attention),
+    which gives the headline value in tokens/s, and
+  * one decode step over a batch of 8 sequences with 1M-token caches (index scan -> top-k
+    -> split-KV sparse attention -> log-sum-exp merge), reported as us/step.
+Inputs are seeded synthetic tensors resident in HBM; L2 is flushed (a 256 MiB write)
+before each timed kernel sequence, outside the timed events.  Times are CUDA events on
+the launching stream.  ``--impl reference`` times the fp64 CPU oracle instead, on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_gqa_02_gb300 import _lib, api  # noqa: E402
+from block_sparse_gqa_02_gb300.configs import CONFIGS  # noqa: E402
+from block_sparse_gqa_02_gb300.inputs import make_inputs  # noqa: E402
+
+METRIC = "MSA prefill tokens/s and decode µs/step at 128K/1M ctx; % of TC/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------- work model
+
+def prefill_flops(cfg):
+    """Algorithmic FLOPs of one prefill: (index, sparse attention), causal pairs only."""
+    T, NI, dI, Hq, d = cfg.seq, cfg.n_heads_kv, cfg.index_dim, cfg.n_heads_q, cfg.head_dim
+    index = T * (T + 1) / 2 * NI * 2 * dI
+    t = np.arange(T, dtype=np.int64)
+    last = np.minimum(T - 1, (t // cfg.q_tile) * cfg.q_tile + cfg.q_tile - 1)
+    cb = last // cfg.block_size
+    keys = (np.minimum(cfg.top_k, cb + 1) - 1) * cfg.block_size + (t - cfg.block_size * cb + 1)
+    sparse = float(keys.sum()) * Hq * 4 * d
+    dense = T * (T + 1) / 2 * Hq * 4 * d
+    return index, sparse, dense
+
+
+def decode_bytes(cfg):
+    """Compulsory HBM bytes of one decode step: (index scan, selected K/V + rest)."""
+    B, L, NI, dI, d, Hq = cfg.batch, cfg.seq, cfg.n_heads_kv, cfg.index_dim, cfg.head_dim, \
+        cfg.n_heads_q
+    nB = -(-L // cfg.block_size)
+    scan = B * L * dI * 2 + B * NI * dI * 2 + B * NI * nB * 4
+    sel_keys = min(cfg.top_k * cfg.block_size, L)
+    kv = B * NI * sel_keys * d * 2 * 2
+    rest = B * NI * nB * 4 + B * Hq * d * 2 * 2 + B * Hq * 4
+    dense = B * NI * L * d * 2 * 2 + B * L * dI * 2
+    return scan, kv + rest, dense
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of the SM clock and throttle reasons while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power)}
+
+
+# -------------------------------------------------------------------- our arm
+
+class Step:
+    """Inputs, outputs and events of one workload, resident on the device."""
+
+    def __init__(self, cfg, device):
+        self.cfg = cfg
+        self.x = make_inputs(cfg, device=device)
+        self.shape = _lib.shape_from_config(cfg)
+        dt = self.x["q"].dtype
+        if cfg.mode == "decode":
+            self.bufs = api.alloc_decode_outputs(self.shape, device, dt)
+            self.kernels = 4
+        else:
+            self.bufs = api.alloc_prefill_outputs(self.shape, device, dt)
+            self.kernels = 3
+        self.ev = []
+
+    def run(self, stream, record=False):
+        x, s, b = self.x, self.shape, self.bufs
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)] if record else None
+        if record:
+            evs[0].record(stream)
+        _lib.msa_index_scores(s, x["idx_q"], x["idx_k"], b["scores"], stream)
+        if record:
+            evs[1].record(stream)
+        _lib.msa_block_topk(s, b["scores"], b["sel"], stream)
+        if record:
+            evs[2].record(stream)
+        if self.cfg.mode == "decode":
+            _lib.msa_sparse_decode(s, x["q"], x["k"], x["v"], b["sel"], b["out"], b["lse"],
+                                   b["ws"], None, stream)
+        else:
+            _lib.msa_sparse_prefill(s, x["q"], x["k"], x["v"], b["sel"], b["out"], b["lse"],
+                                    None, 0, stream)
+        if record:
+            evs[3].record(stream)
+            self.ev.append(evs)
+
+    def times_ms(self):
+        """Per step: (total, index, topk, attention) in ms."""
+        out = []
+        for e in self.ev:
+            out.append((e[0].elapsed_time(e[3]), e[0].elapsed_time(e[1]),
+                        e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])))
+        return np.array(out)
+
+
+def e2e_prefill(cfg, step, stream, n_steps):
+    """The same metric through the public API with host buffers: pinned H2D copies of the
+    step's inputs, the three library calls, D2H of out and lse, per step."""
+    names = ["q", "k", "v", "idx_q", "idx_k"]
+    host = {n: step.x[n].cpu().pin_memory() for n in names}
+    out_h = torch.empty(step.bufs["out"].shape, dtype=step.bufs["out"].dtype).pin_memory()
+    lse_h = torch.empty(step.bufs["lse"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    dev = {n: torch.empty_like(step.x[n]) for n in names}
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(n_steps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for n in names:
+                dev[n].copy_(host[n], non_blocking=True)
+            api.run_prefill(step.shape, dev["q"], dev["k"], dev["v"], dev["idx_q"],
+                            dev["idx_k"], step.bufs, stream)
+            out_h.copy_(step.bufs["out"], non_blocking=True)
+            lse_h.copy_(step.bufs["lse"], non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            if i > 0:                       # first pass warms the copy engines
+                times.append(e0.elapsed_time(e1))
+    ms = float(np.mean(times))
+    return {"value": cfg.seq * cfg.batch / (ms / 1e3), "unit": "tokens/s",
+            "ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": n_steps}, host
+
+
+def cpu_baseline_prefill(cfg, host, budget_s=15.0, seed=0):
+    """The oracle as it stands on the host cores, on uniformly sampled query tiles of the
+    same prefill (all heads); tokens/s = q_tile * tiles / time, an unbiased estimate of
+    the whole pass because tiles are drawn uniformly."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    n_tiles = -(-cfg.seq // cfg.q_tile)
+    done, t0 = [], time.perf_counter()
+    while (time.perf_counter() - t0 < budget_s and len(done) < 64) or len(done) < 2:
+        m = int(rng.integers(0, n_tiles))
+        oracle.msa_prefill(host["q"], host["k"], host["v"], host["idx_q"], host["idx_k"],
+                           cfg.block_size, cfg.q_tile, cfg.top_k, tiles=[m])
+        done.append(m)
+    el = time.perf_counter() - t0
+    return {"value": cfg.q_tile * len(done) / el, "unit": "tokens/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"{len(done)} uniformly drawn 64-query tiles of the {cfg.name} prefill, "
+                      f"all heads, fp64 numpy; extrapolated to tokens/s over {el:.1f} s"}
+
+
+def run_ours(args, rank, world, device):
+    torch.cuda.set_device(device)
+    _lib.load()
+    pcfg = CONFIGS[args.prefill]
+    dcfg = CONFIGS[args.decode]
+    stream = torch.cuda.Stream(device)
+    pre = Step(pcfg, device)
+    dec = Step(dcfg, device) if not args.no_decode else None
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=device)   # 256 MiB > L2
+    torch.cuda.synchronize()
+
+    def one(step, record):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        step.run(stream, record)
+
+    for _ in range(args.warmup):
+        one(pre, False)
+        if dec:
+            one(dec, False)
+    _lib.msa_get_device_status(stream)
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        one(pre, True)
+        if dec:
+            one(dec, True)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    _lib.msa_get_device_status(stream)
+
+    pt = pre.times_ms()
+    dt = dec.times_ms() if dec else None
+    pre_ms = float(pt[:, 0].sum())
+    if world > 1:
+        t = torch.tensor([pre_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        pre_ms = float(t.item())
+    if rank != 0:
+        return None
+
+    peaks, peak_src = load_peaks()
+    tc_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    hbm_peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    f_index, f_sparse, f_dense = prefill_flops(pcfg)
+    k_idx, k_topk, k_attn = (float(pt[:, i].mean()) for i in (1, 2, 3))
+    tokens = pcfg.seq * pcfg.batch
+    value = world * tokens * args.steps / (pre_ms / 1e3)
+    attn_tf = f_sparse / (k_attn / 1e3) / 1e12
+    idx_tf = f_index / (k_idx / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": pre_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{pcfg.name}: {pcfg.description}"
+                               + (f" | decode {dcfg.name}: {dcfg.description}" if dec else ""),
+                   "global_batch": pcfg.batch * world, "seq_len": pcfg.seq,
+                   "parallelism": "replicas" if world > 1 else "single-gpu",
+                   "l2": "flushed by a 256 MiB write before every timed kernel sequence",
+                   "timing": "CUDA events on the launching stream around the library calls"},
+        "roofline": {"bound": "tensor", "kernel": "sparse prefill attention",
+                     "achieved": attn_tf, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": attn_tf / tc_peak, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 sustained",
+                     "algorithmic_flops_per_launch": f_sparse},
+        "kernels_ms": {"index_scores": k_idx, "block_topk": k_topk, "sparse_prefill": k_attn},
+        "index_roofline": {"bound": "tensor", "achieved": idx_tf, "peak": tc_peak,
+                           "unit": "TFLOP/s", "frac": idx_tf / tc_peak,
+                           "algorithmic_flops_per_launch": f_index},
+        "dense_flops_avoided": f_dense - f_sparse,
+        "msa_prefill_tflops_per_s": (f_index + f_sparse) / (pre_ms / args.steps / 1e3) / 1e12,
+        "clocks": clk,
+        "gpu_launches": args.steps * (pre.kernels + (dec.kernels if dec else 0)),
+        "wall_s_timed_region": wall,
+    }
+    if dec:
+        b_scan, b_rest, b_dense = decode_bytes(dcfg)
+        d_idx, d_topk, d_attn = (float(dt[:, i].mean()) for i in (1, 2, 3))
+        d_total = float(dt[:, 0].mean())
+        scan_gbs = b_scan / (d_idx / 1e3) / 1e9
+        line["decode"] = {
+            "us_per_step": d_total * 1e3, "unit": "us/step", "higher_is_better": False,
+            "workload": f"{dcfg.name}: {dcfg.description}",
+            "kernels_us": {"index_scan": d_idx * 1e3, "block_topk": d_topk * 1e3,
+                           "sparse_decode+combine": d_attn * 1e3},
+            "roofline": {"bound": "hbm", "kernel": "decode index scan", "achieved": scan_gbs,
+                         "peak": hbm_peak, "unit": "GB/s", "frac": scan_gbs / hbm_peak,
+                         "traffic": None, "algorithmic_bytes_per_launch": b_scan},
+            "step_hbm_gbs": (b_scan + b_rest) / (d_total / 1e3) / 1e9,
+            "dense_bytes_avoided": b_dense - (b_scan + b_rest),
+        }
+    if not args.no_e2e:
+        e2e, host = e2e_prefill(pcfg, pre, stream, max(2, min(args.steps, 5)))
+        line["e2e"] = e2e
+    else:
+        host = {n: pre.x[n].cpu() for n in ["q", "k", "v", "idx_q", "idx_k"]}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline_prefill(pcfg, host, args.cpu_budget)
+    return line
+
+
+# --------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The fp64 oracle as it stands, timed on the host cores on the same workload: each
+    step is one uniformly drawn 64-query tile of the prefill (all heads)."""
+    import oracle
+    cfg = CONFIGS[args.prefill]
+    x = make_inputs(cfg, device="cpu")
+    rng = np.random.default_rng(1)
+    n_tiles = -(-cfg.seq // cfg.q_tile)
+    times = []
+    for i in range(args.warmup + args.steps):
+        m = int(rng.integers(0, n_tiles))
+        t0 = time.perf_counter()
+        oracle.msa_prefill(x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"], cfg.block_size,
+                           cfg.q_tile, cfg.top_k, tiles=[m])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    sec = float(np.mean(times))
+    value = cfg.q_tile / sec
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: {cfg.description}", "global_batch": cfg.batch,
+                   "seq_len": cfg.seq, "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"one uniformly drawn 64-query tile of the {cfg.name} "
+                                   "prefill per step, all heads, fp64 numpy"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
+    ap.add_argument("--prefill", default="p128k", choices=["p32k", "p128k", "p1m"])
+    ap.add_argument("--decode", default="d1m", choices=["d1m"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = run_ours(args, rank, world, torch.device("cuda", local))
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

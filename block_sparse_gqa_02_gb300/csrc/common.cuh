@@ -1,0 +1,80 @@
+// Internal declarations shared by the MSA kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+namespace msa {
+
+// Shape after validation, with the derived sizes every kernel needs.
+struct Dims {
+  int B, Sq, Sk, Hq, Hkv, G, d, dI, Bk, k, Qt;
+  int nB;        // ceil(Sk / Bk): blocks per sequence
+  int nR;        // ceil(Sq / Qt): selection rows per (sequence, KV head)
+  int q_off;     // position of query 0 (0 for prefill, Sk - 1 for decode)
+  int decode;    // 1 when Sq == 1 and Qt == 1
+  int dtype;     // 0 f32, 1 bf16
+  float sm_scale, index_scale;
+};
+
+// Position of the last query of selection row m; its block is the row's current block.
+__host__ __device__ inline int row_last_pos(const Dims& p, int m) {
+  int last = m * p.Qt + p.Qt - 1;
+  if (last > p.Sq - 1) last = p.Sq - 1;
+  return p.q_off + last;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+
+// 16-byte vector of T converted to fp32 (4 floats or 8 bf16 -> 8 floats).
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const float* p, float* o) {
+    float4 x = *reinterpret_cast<const float4*>(p);
+    o[0] = x.x; o[1] = x.y; o[2] = x.z; o[3] = x.w;
+  }
+};
+template <> struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const __nv_bfloat16* p, float* o) {
+    uint4 x = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+// ----------------------------------------------------------------- launchers
+// Each returns the launch error (cudaSuccess when the kernel was queued).
+cudaError_t launch_index_scores(const Dims& p, const void* idx_q, const void* idx_k,
+                                float* scores, cudaStream_t st, int* dev_status);
+cudaError_t launch_block_topk(const Dims& p, const float* scores, int32_t* sel,
+                              cudaStream_t st);
+cudaError_t launch_sparse_prefill(const Dims& p, const void* q, const void* k,
+                                  const void* v, const int32_t* sel, void* out, float* lse,
+                                  cudaStream_t st, int* dev_status);
+cudaError_t launch_sparse_decode(const Dims& p, const void* q, const void* k, const void* v,
+                                 const int32_t* sel, void* out, float* lse, float* ws,
+                                 cudaStream_t st);
+
+// Decode split-KV: number of block groups each (sequence, KV head) is split into, and
+// the scratch it needs (partial outputs and partial log-sum-exps, fp32).
+int decode_num_splits(const Dims& p);
+size_t decode_workspace_bytes(const Dims& p);
+
+// Largest candidate count the top-k kernel keeps in shared memory.
+constexpr int kMaxBlocks = 32768;
+
+}  // namespace msa

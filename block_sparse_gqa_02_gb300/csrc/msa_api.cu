@@ -1,0 +1,239 @@
+// C-ABI entry points of the MSA library (declared in include/msa.h): argument checks,
+// shape derivation, dispatch to the kernels, error reporting.  No entry point allocates.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "msa.h"
+
+namespace msa {
+
+// Device status word: kernels that give up a bounded wait write a nonzero code here.
+__device__ int g_device_status = 0;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+msa_status fail(msa_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+msa_status fail(msa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+msa_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(MSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+int* status_ptr() {
+  static thread_local int dev = -1;
+  static thread_local int* ptr = nullptr;
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) return nullptr;
+  if (dev != cur) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    ptr = static_cast<int*>(p);
+    dev = cur;
+  }
+  return ptr;
+}
+
+// Validates the shape and derives the kernel dimensions.
+msa_status make_dims(const msa_shape* s, Dims* d) {
+  if (!s) return fail(MSA_ERR_INVALID_ARG, "shape is NULL");
+  if (s->batch < 1 || s->seq_q < 1 || s->seq_k < 1)
+    return fail(MSA_ERR_INVALID_ARG, "batch, seq_q and seq_k must be >= 1 (got %d, %d, %d)",
+                s->batch, s->seq_q, s->seq_k);
+  if (s->n_heads_kv < 1 || s->n_heads_q < 1 || s->n_heads_q % s->n_heads_kv != 0)
+    return fail(MSA_ERR_INVALID_ARG, "n_heads_q (%d) must be a positive multiple of n_heads_kv (%d)",
+                s->n_heads_q, s->n_heads_kv);
+  if (s->block_size < 1 || s->top_k < 1 || s->q_tile < 1)
+    return fail(MSA_ERR_INVALID_ARG, "block_size, top_k and q_tile must be >= 1");
+  if (s->dtype != MSA_F32 && s->dtype != MSA_BF16)
+    return fail(MSA_ERR_INVALID_ARG, "dtype must be MSA_F32 or MSA_BF16 (got %d)", s->dtype);
+  if (!(s->sm_scale >= 0.f) || !(s->index_scale >= 0.f) || isinf(s->sm_scale) ||
+      isinf(s->index_scale))
+    return fail(MSA_ERR_INVALID_ARG, "sm_scale and index_scale must be finite and >= 0");
+  const bool decode = s->seq_q == 1 && s->q_tile == 1;
+  if (!decode) {
+    if (s->seq_q != s->seq_k)
+      return fail(MSA_ERR_INVALID_ARG,
+                  "prefill needs seq_q == seq_k (got %d, %d); decode needs seq_q == q_tile == 1",
+                  s->seq_q, s->seq_k);
+    if (s->block_size % s->q_tile != 0)
+      return fail(MSA_ERR_INVALID_ARG, "block_size (%d) must be a multiple of q_tile (%d)",
+                  s->block_size, s->q_tile);
+  }
+  if (s->head_dim != 64 && s->head_dim != 128)
+    return fail(MSA_ERR_UNSUPPORTED, "head_dim %d: supported 64, 128", s->head_dim);
+  if (s->index_dim != 64 && s->index_dim != 128)
+    return fail(MSA_ERR_UNSUPPORTED, "index_dim %d: supported 64, 128", s->index_dim);
+  const long long nB = ((long long)s->seq_k + s->block_size - 1) / s->block_size;
+  if (nB > kMaxBlocks)
+    return fail(MSA_ERR_UNSUPPORTED, "%lld blocks per sequence: at most %d", nB, kMaxBlocks);
+  d->B = s->batch;
+  d->Sq = s->seq_q;
+  d->Sk = s->seq_k;
+  d->Hq = s->n_heads_q;
+  d->Hkv = s->n_heads_kv;
+  d->G = s->n_heads_q / s->n_heads_kv;
+  d->d = s->head_dim;
+  d->dI = s->index_dim;
+  d->Bk = s->block_size;
+  d->k = s->top_k;
+  d->Qt = s->q_tile;
+  d->nB = (int)nB;
+  d->nR = (s->seq_q + s->q_tile - 1) / s->q_tile;
+  d->q_off = decode ? s->seq_k - 1 : 0;
+  d->decode = decode ? 1 : 0;
+  d->dtype = s->dtype;
+  d->sm_scale = s->sm_scale > 0.f ? s->sm_scale : 1.f / sqrtf((float)s->head_dim);
+  d->index_scale = s->index_scale > 0.f ? s->index_scale : 1.f / sqrtf((float)s->index_dim);
+  return MSA_OK;
+}
+
+msa_status check_ptr(const void* p, const char* name, bool nullable = false) {
+  if (!p) return nullable ? MSA_OK : fail(MSA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(MSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return MSA_OK;
+}
+
+#define MSA_TRY(expr)                    \
+  do {                                   \
+    msa_status st_ = (expr);             \
+    if (st_ != MSA_OK) return st_;       \
+  } while (0)
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+msa_status msa_index_scores(const msa_shape* shape, const void* idx_q, const void* idx_k,
+                            float* block_scores, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  MSA_TRY(check_ptr(idx_q, "idx_q"));
+  MSA_TRY(check_ptr(idx_k, "idx_k"));
+  MSA_TRY(check_ptr(block_scores, "block_scores"));
+  if (!d.decode && d.Hkv * d.Qt > 256 && d.dtype == MSA_F32)
+    return fail(MSA_ERR_UNSUPPORTED, "fp32 index scores need n_heads_kv * q_tile <= 256");
+  if (d.decode && d.Hkv != 1 && d.Hkv != 2 && d.Hkv != 4 && d.Hkv != 8)
+    return fail(MSA_ERR_UNSUPPORTED, "decode index scan needs n_heads_kv in {1, 2, 4, 8}");
+  if (!d.decode && d.dtype == MSA_BF16 && d.Hkv * d.Qt > 256)
+    return fail(MSA_ERR_UNSUPPORTED, "index scores need n_heads_kv * q_tile <= 256");
+  if (!d.decode && (size_t)d.Bk * d.dI * sizeof(float) > 200 * 1024)
+    return fail(MSA_ERR_UNSUPPORTED, "index scores stage one key block (%d x %d fp32) in "
+                "shared memory: at most 200 KiB", d.Bk, d.dI);
+  cudaError_t e = launch_index_scores(d, idx_q, idx_k, block_scores, (cudaStream_t)stream,
+                                      status_ptr());
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_scores launch");
+}
+
+msa_status msa_block_topk(const msa_shape* shape, const float* block_scores, int32_t* sel,
+                          void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  MSA_TRY(check_ptr(block_scores, "block_scores"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  cudaError_t e = launch_block_topk(d, block_scores, sel, (cudaStream_t)stream);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_block_topk launch");
+}
+
+msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void* k,
+                              const void* v, const int32_t* sel, void* out, float* lse,
+                              void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  (void)workspace;
+  (void)ws_bytes;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  if (d.decode && d.Sk != 1)
+    return fail(MSA_ERR_INVALID_ARG, "msa_sparse_prefill needs seq_q == seq_k; use msa_sparse_decode");
+  MSA_TRY(check_ptr(q, "q"));
+  MSA_TRY(check_ptr(k, "k"));
+  MSA_TRY(check_ptr(v, "v"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  MSA_TRY(check_ptr(out, "out"));
+  MSA_TRY(check_ptr(lse, "lse", true));
+  cudaError_t e = launch_sparse_prefill(d, q, k, v, sel, out, lse, (cudaStream_t)stream,
+                                        status_ptr());
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_prefill launch");
+}
+
+msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* sel, void* out, float* lse,
+                             void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  if (!d.decode) return fail(MSA_ERR_INVALID_ARG, "msa_sparse_decode needs seq_q == q_tile == 1");
+  if (d.G > 64) return fail(MSA_ERR_UNSUPPORTED, "decode needs n_heads_q / n_heads_kv <= 64");
+  MSA_TRY(check_ptr(q, "q"));
+  MSA_TRY(check_ptr(k_cache, "k_cache"));
+  MSA_TRY(check_ptr(v_cache, "v_cache"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  MSA_TRY(check_ptr(out, "out"));
+  MSA_TRY(check_ptr(lse, "lse", true));
+  MSA_TRY(check_ptr(workspace, "workspace"));
+  const size_t need = decode_workspace_bytes(d);
+  if (ws_bytes < need)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes is too small: need %zu", ws_bytes,
+                need);
+  cudaError_t e = launch_sparse_decode(d, q, k_cache, v_cache, sel, out, lse,
+                                       static_cast<float*>(workspace), (cudaStream_t)stream);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode launch");
+}
+
+size_t msa_workspace_bytes(const msa_shape* shape, int which) {
+  Dims d;
+  if (make_dims(shape, &d) != MSA_OK) return 0;
+  if (which == 1 && d.decode) return decode_workspace_bytes(d);
+  return 0;
+}
+
+msa_status msa_get_device_status(void* stream) {
+  g_last_error[0] = 0;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "pending CUDA error");
+  int code = 0;
+  e = cudaMemcpyFromSymbol(&code, g_device_status, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "read device status");
+  if (code != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    return fail(MSA_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", code);
+  }
+  return MSA_OK;
+}
+
+const char* msa_status_string(msa_status status) {
+  switch (status) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_ERR_INVALID_ARG: return "MSA_ERR_INVALID_ARG: invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED: shape not supported";
+    case MSA_ERR_CUDA: return "MSA_ERR_CUDA: CUDA error";
+    case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+  }
+  return "unknown msa_status";
+}
+
+const char* msa_last_error(void) { return g_last_error; }
+
+int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
+
+}  // extern "C"

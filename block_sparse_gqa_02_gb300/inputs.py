@@ -120,3 +120,29 @@ def random_selection(n_candidates: np.ndarray, top_k: int, seed: int) -> np.ndar
         chosen = np.sort(np.concatenate([others, [cur]]).astype(np.int32))
         out[idx][: len(chosen)] = chosen
     return out
+
+
+def random_block_scores(shape, seed: int, kind: str = "normal") -> np.ndarray:
+    """fp32 block-score tensors for testing the top-k step on its own.
+
+    kind "normal": N(0,1); "ties": small integers (many equal scores, both signed zeros);
+    "mixed": normal values with runs of repeated values and signed zeros spliced in.
+    """
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        x = rng.standard_normal(shape)
+    elif kind == "ties":
+        x = rng.integers(-3, 4, size=shape).astype(np.float64)
+        zero = x == 0
+        x[zero] = np.where(rng.random(int(zero.sum())) < 0.5, 0.0, -0.0)
+    elif kind == "mixed":
+        x = rng.standard_normal(shape)
+        flat = x.reshape(-1)
+        n = flat.size
+        pick = rng.integers(0, n, size=max(1, n // 8))
+        flat[pick] = flat[rng.integers(0, n, size=pick.size)]
+        flat[rng.integers(0, n, size=max(1, n // 64))] = 0.0
+        flat[rng.integers(0, n, size=max(1, n // 64))] = -0.0
+    else:
+        raise ValueError(kind)
+    return x.astype(np.float32)

@@ -1,0 +1,140 @@
+/*
+ * msa.h -- C ABI of the MiniMax Sparse Attention (MSA) hot path for GB300 (sm_103a).
+ *
+ * The method (from the talk pages on MSA):
+ *   - an index branch runs lightweight causal full attention with one index query head
+ *     per KV head against ONE shared index key head, and its scores are reduced to
+ *     per-key-block scores ("Sparse Attention Cannot Be Directly Ported Across
+ *     Architectures", disconfirmai.com, paragraph introducing MSA; "How MiniMax M3 was
+ *     built", aietalks.com, section "MSA uses a lightweight index branch before sparse
+ *     attention");
+ *   - every KV head takes its own top-k of blocks, never merged across heads (same
+ *     article, paragraph "MSA addresses these issues"; aietalks.com, section
+ *     "Block-level retrieval makes sparse attention easier to run on GPUs");
+ *   - the main GQA branch computes exact softmax attention over the selected blocks only
+ *     (Chinese topic page on MSA, summary paragraph).
+ * The pages fix no block size, k, pooling or tie-break; this library uses: scores are the
+ * MAX over a query tile's tokens and a block's causally visible keys of
+ * index_scale * <q_I, k_I>; the block holding the tile's last query (the "current block")
+ * is always selected and counts towards top_k; the other top_k-1 are the highest scores,
+ * ties to the lower block index, -0 == +0; the list is written ascending, padded with -1.
+ *
+ * Layouts (row-major, contiguous, element type = shape->dtype unless stated):
+ *   q, out        [batch, seq_q, n_heads_q, head_dim]
+ *   k, v          [batch, n_heads_kv, seq_k, head_dim]    (head-major: a block of one
+ *                                                          KV head is one contiguous run)
+ *   idx_q         [batch, seq_q, n_heads_kv, index_dim]   (index query head g serves KV head g)
+ *   idx_k         [batch, seq_k, index_dim]               (the single index key head)
+ *   block_scores  float32 [batch, n_heads_kv, n_rows, n_blocks]
+ *   sel           int32   [batch, n_heads_kv, n_rows, top_k]
+ *   lse           float32 [batch, n_heads_q, seq_q], natural log
+ * with n_blocks = ceil(seq_k / block_size) and n_rows = ceil(seq_q / q_tile).
+ *
+ * Two modes, told apart by the shape:
+ *   prefill  seq_q == seq_k == T, query i at position i, rows are tiles of q_tile queries
+ *            (block_size % q_tile == 0);
+ *   decode   seq_q == 1, q_tile == 1, seq_k == L (the cache includes the new token), the
+ *            query at position L-1, one row per sequence (selection per token).
+ * Query head h uses KV head h / (n_heads_q / n_heads_kv).
+ *
+ * Conventions:
+ *   - Ownership: the caller owns every buffer.  Only msa_sparse_decode needs scratch, and
+ *     the caller passes it (msa_workspace_bytes); no entry point here allocates memory.
+ *   - Pointers are device pointers (cudaMalloc or equivalent), 16-byte aligned.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns after launching.  Argument checks happen before any launch; on
+ *     failure nothing is launched and msa_last_error() describes the problem.
+ *   - A kernel that gives up a bounded wait sets a device status word that
+ *     msa_get_device_status() reports as MSA_ERR_TIMEOUT.
+ *   - Inputs must be finite; NaN scores give an unspecified (but in-range) selection.
+ *   - Calls on distinct streams may run concurrently; the device status word is shared.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MSA_ABI_VERSION 1
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, inconsistent or out-of-range shape */
+  MSA_ERR_UNSUPPORTED = 2, /* valid shape that no kernel here handles (e.g. head_dim 96) */
+  MSA_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+  MSA_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (device status word) */
+} msa_status;
+
+typedef enum msa_dtype { MSA_F32 = 0, MSA_BF16 = 1 } msa_dtype;
+
+typedef struct msa_shape {
+  int32_t batch;       /* B >= 1 */
+  int32_t seq_q;       /* prefill: T; decode: 1 */
+  int32_t seq_k;       /* prefill: T; decode: cache length L >= 1 */
+  int32_t n_heads_q;   /* Hq, a multiple of n_heads_kv */
+  int32_t n_heads_kv;  /* Hkv = number of index query heads */
+  int32_t head_dim;    /* d: 64 or 128 */
+  int32_t index_dim;   /* dI: 64 or 128 */
+  int32_t block_size;  /* keys per block, >= 1 */
+  int32_t top_k;       /* blocks per KV head, current block included, >= 1 */
+  int32_t q_tile;      /* queries sharing one selection: prefill divides block_size; decode 1 */
+  int32_t dtype;       /* msa_dtype of q, k, v, idx_q, idx_k, out */
+  float sm_scale;      /* softmax scale; 0 means 1/sqrt(head_dim) */
+  float index_scale;   /* index logit scale; 0 means 1/sqrt(index_dim) */
+} msa_shape;
+
+/* Index branch: block_scores[b, g, m, blk] = max over the queries t of row m and the keys
+ * j <= t of block blk of index_scale * <idx_q[b, t, g, :], idx_k[b, j, :]>; -inf for blocks
+ * with no visible key.  Accumulation is fp32.  Prefill uses tcgen05 tensor cores for
+ * bf16 with index_dim 128; decode is a streaming scan of the index-key cache. */
+msa_status msa_index_scores(const msa_shape* shape, const void* idx_q, const void* idx_k,
+                            float* block_scores, void* stream);
+
+/* Per-KV-head block top-k of block_scores (layout above) into sel: the current block plus
+ * the best top_k-1 of the earlier blocks by (score desc, index asc), ascending, -1 padded.
+ * Bit-exact and deterministic.  Rows may hold up to 32768 candidate blocks. */
+msa_status msa_block_topk(const msa_shape* shape, const float* block_scores, int32_t* sel,
+                          void* stream);
+
+/* Main branch, prefill (seq_q == seq_k): for query t and head h (KV head g), attend over the
+ * keys j <= t of the blocks listed in sel[b, g, t / q_tile, :] (entries -1 are skipped;
+ * entries must be distinct).  Writes out (dtype) and, if lse != NULL, lse.  A row whose key
+ * set is empty gets out = 0 and lse = -inf.  workspace may be NULL (ws_bytes 0). */
+msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void* k,
+                              const void* v, const int32_t* sel, void* out, float* lse,
+                              void* workspace, size_t ws_bytes, void* stream);
+
+/* Main branch, decode (seq_q == 1, q_tile == 1): the new token of every sequence attends
+ * over the selected blocks of the cache (split over the blocks, partial results merged by
+ * log-sum-exp).  workspace: device scratch of at least msa_workspace_bytes(shape, 1)
+ * bytes, 16-byte aligned, owned by the caller; its contents on entry do not matter. */
+msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* k_cache,
+                             const void* v_cache, const int32_t* sel, void* out, float* lse,
+                             void* workspace, size_t ws_bytes, void* stream);
+
+/* Scratch bytes msa_sparse_prefill (which = 0) or msa_sparse_decode (which = 1) needs for
+ * this shape; 0 when none.  Returns 0 for an invalid shape. */
+size_t msa_workspace_bytes(const msa_shape* shape, int which);
+
+/* Synchronises `stream`, then reports (and clears) the device status word and any pending
+ * CUDA error: MSA_OK, MSA_ERR_TIMEOUT or MSA_ERR_CUDA. */
+msa_status msa_get_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* msa_status_string(msa_status status);
+
+/* Human-readable detail of the last failure on the calling thread ("" if none). */
+const char* msa_last_error(void);
+
+/* MSA_ABI_VERSION of the loaded library. */
+int32_t msa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -46,6 +46,21 @@ def _f64(x) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
+def _rows(x, *index) -> np.ndarray:
+    """x[index] as a float64 numpy array; x is a numpy array or a torch tensor on any
+    device.  Only the requested slice is converted, so large caches never are."""
+    if hasattr(x, "detach"):
+        import torch
+        idx = tuple(torch.as_tensor(i, device=x.device) if isinstance(i, np.ndarray) else i
+                    for i in index)
+        return x[idx].detach().to("cpu").double().numpy()
+    return np.asarray(np.asarray(x)[index], dtype=np.float64)
+
+
+# Index keys are scored this many blocks at a time (the scores are defined per block).
+_BLOCKS_PER_CHUNK = 256
+
+
 def default_scale(dim: int) -> float:
     """Softmax scale used when a caller passes 0: 1/sqrt(dim)."""
     return 1.0 / np.sqrt(dim)
@@ -55,19 +70,20 @@ def default_scale(dim: int) -> float:
 # Index branch: causal index logits, max-pooled per (query tile, key block)
 # ---------------------------------------------------------------------------
 
-def index_logits(idx_q_rows, idx_k, index_scale, q_pos):
+def index_logits(idx_q_rows, idx_k, index_scale, q_pos, key_pos0=0):
     """Causal index logits for a set of query tokens.
 
     idx_q_rows [n, NI, dI] are the index queries of n tokens at positions q_pos[n];
-    idx_k [L, dI] is the single shared index key head.  Returns s [NI, n, L] with
-    s[g, i, j] = index_scale * <idx_q_rows[i, g], idx_k[j]> for j <= q_pos[i] and -inf
-    for j > q_pos[i] (four index query heads against one key head: the MSA paragraph of
-    the disconfirmai.com article).
+    idx_k [L, dI] holds the single shared index key head at positions key_pos0 ..
+    key_pos0 + L - 1.  Returns s [NI, n, L] with s[g, i, j] = index_scale *
+    <idx_q_rows[i, g], idx_k[j]> where key j is visible (position <= q_pos[i]) and -inf
+    elsewhere (four index query heads against one key head: the MSA paragraph of the
+    disconfirmai.com article).
     """
     qr = _f64(idx_q_rows)
     kk = _f64(idx_k)
-    s = index_scale * np.einsum("ngc,jc->gnj", qr, kk)
-    j = np.arange(kk.shape[0])
+    s = index_scale * np.matmul(qr.transpose(1, 0, 2), kk.T)          # [NI, n, L]
+    j = key_pos0 + np.arange(kk.shape[0])
     visible = j[None, :] <= np.asarray(q_pos)[:, None]          # [n, L]
     return np.where(visible[None, :, :], s, -np.inf)
 
@@ -86,6 +102,24 @@ def pool_blocks(s, block_size):
     return s.reshape(NI, n, nB, block_size).max(axis=(1, 3))
 
 
+def _pooled_row(q_rows, idx_k_b, index_scale, q_pos, block_size, n_blocks):
+    """Block scores [NI, n_blocks] of a group of query tokens against one sequence's keys.
+
+    Blocks that hold no key visible to any of the tokens score -inf; the others are
+    pooled chunk by chunk of whole blocks.
+    """
+    NI = q_rows.shape[1]
+    out = np.full((NI, n_blocks), -np.inf)
+    n_visible = int(np.max(q_pos)) + 1                  # keys 0 .. max position
+    vis_blocks = -(-n_visible // block_size)
+    for c0 in range(0, vis_blocks, _BLOCKS_PER_CHUNK):
+        c1 = min(vis_blocks, c0 + _BLOCKS_PER_CHUNK)
+        j0, j1 = c0 * block_size, min(n_visible, c1 * block_size)
+        s = index_logits(q_rows, _rows(idx_k_b, slice(j0, j1)), index_scale, q_pos, j0)
+        out[:, c0:c1] = pool_blocks(s, block_size)
+    return out
+
+
 def index_block_scores_prefill(idx_q, idx_k, block_size, q_tile, index_scale=None,
                                tiles=None):
     """Prefill block scores S[b, g, m, blk] for query tiles m of q_tile tokens.
@@ -95,8 +129,7 @@ def index_block_scores_prefill(idx_q, idx_k, block_size, q_tile, index_scale=Non
     keys j <= t, of the scaled index logit; -inf when no key of the block is visible.
     ``tiles`` restricts the result to a list of tile indices (axis 2 follows that list).
     """
-    qi, ki = _f64(idx_q), _f64(idx_k)
-    B, T, NI, dI = qi.shape
+    B, T, NI, dI = idx_q.shape
     if index_scale is None or index_scale == 0:
         index_scale = default_scale(dI)
     nT = -(-T // q_tile)
@@ -106,8 +139,8 @@ def index_block_scores_prefill(idx_q, idx_k, block_size, q_tile, index_scale=Non
     for b in range(B):
         for col, m in enumerate(tile_list):
             t = np.arange(m * q_tile, min(T, (m + 1) * q_tile))
-            s = index_logits(qi[b, t], ki[b], index_scale, t)
-            out[b, :, col, :] = pool_blocks(s, block_size)
+            q_rows = _rows(idx_q, b, slice(int(t[0]), int(t[-1]) + 1))
+            out[b, :, col, :] = _pooled_row(q_rows, idx_k[b], index_scale, t, block_size, nB)
     return out
 
 
@@ -117,16 +150,16 @@ def index_block_scores_decode(idx_q, idx_k, block_size, index_scale=None):
     idx_q [B, 1, NI, dI] (the new token's index queries), idx_k [B, L, dI] (the index-key
     cache, the new token included).  Selection is per token in decode.
     """
-    qi, ki = _f64(idx_q), _f64(idx_k)
-    B, _, NI, dI = qi.shape
-    L = ki.shape[1]
+    B, _, NI, dI = idx_q.shape
+    L = idx_k.shape[1]
     if index_scale is None or index_scale == 0:
         index_scale = default_scale(dI)
     nB = -(-L // block_size)
     out = np.empty((B, NI, 1, nB))
     for b in range(B):
-        s = index_logits(qi[b, 0:1], ki[b], index_scale, np.array([L - 1]))
-        out[b, :, 0, :] = pool_blocks(s, block_size)
+        q_rows = _rows(idx_q, b, slice(0, 1))
+        out[b, :, 0, :] = _pooled_row(q_rows, idx_k[b], index_scale, np.array([L - 1]),
+                                      block_size, nB)
     return out
 
 
@@ -214,9 +247,8 @@ def sparse_attention(q, k, v, sel, block_size, q_tile, sm_scale=None, q_offset=0
 
     Returns (out [B, Sq, Hq, d] or only the listed tiles' rows, lse [B, Hq, Sq or rows]).
     """
-    qf, kf, vf = _f64(q), _f64(k), _f64(v)
-    B, Sq, Hq, d = qf.shape
-    Hkv, Sk = kf.shape[1], kf.shape[2]
+    B, Sq, Hq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
     G = Hq // Hkv
     if sm_scale is None or sm_scale == 0:
         sm_scale = default_scale(d)
@@ -235,9 +267,9 @@ def sparse_attention(q, k, v, sel, block_size, q_tile, sm_scale=None, q_offset=0
                 J = selected_keys(sel[b, g, m], block_size, Sk)
                 if J.size == 0:
                     continue
-                heads = np.arange(g * G, (g + 1) * G)
-                z = sm_scale * np.einsum("thc,jc->thj", qf[b][np.ix_(t_idx, heads)],
-                                         kf[b, g, J])
+                q_rows = _rows(q, b, slice(int(t_idx[0]), int(t_idx[-1]) + 1),
+                               slice(g * G, (g + 1) * G))                     # [n, G, d]
+                z = sm_scale * np.matmul(q_rows, _rows(k, b, g, J).T)        # [n, G, |J|]
                 z = np.where((J[None, None, :] <= pos[:, None, None]), z, -np.inf)
                 zmax = z.max(axis=2, keepdims=True)
                 has = np.isfinite(zmax[..., 0])
@@ -247,7 +279,7 @@ def sparse_attention(q, k, v, sel, block_size, q_tile, sm_scale=None, q_offset=0
                 with np.errstate(divide="ignore", invalid="ignore"):
                     l = np.where(has, np.log(ssum) + zmax[..., 0], -np.inf)
                     p = np.where(has[..., None], e / ssum[..., None], 0.0)
-                o = np.einsum("thj,jc->thc", p, vf[b, g, J])
+                o = np.matmul(p, _rows(v, b, g, J))                          # [n, G, d]
                 out[b, r0:r0 + len(t_idx), g * G:(g + 1) * G, :] = o
                 lse[b, g * G:(g + 1) * G, r0:r0 + len(t_idx)] = l.T
         r0 += len(t_idx)

@@ -1,0 +1,296 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, element by element.
+
+Each stage is tested on its own with seeded inputs from the generator (so no oracle
+input ever comes from the CUDA path), and the three stages are tested chained.  Small
+ragged shapes are compared in full; the full-size configurations are run in full on the
+GPU, in the launch configuration the benchmark times, and compared on sampled tiles.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_gqa_02_gb300 import _lib
+from block_sparse_gqa_02_gb300.api import (alloc_decode_outputs, alloc_prefill_outputs,
+                                           run_decode, run_prefill)
+from block_sparse_gqa_02_gb300.configs import CONFIGS
+from block_sparse_gqa_02_gb300.inputs import (make_inputs, random_block_scores,
+                                              random_selection)
+from tests.parity import (check_lse, check_out, check_scores, check_selection_valid,
+                          sample_tiles, to_np)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def cur_blocks(shape):
+    """Current block of every selection row (oracle's rule)."""
+    if shape.seq_q == 1 and shape.q_tile == 1:
+        return np.array([oracle.current_block(shape.seq_k - 1, shape.block_size)])
+    return np.array([oracle.current_block(min(shape.seq_q - 1, m * shape.q_tile + shape.q_tile - 1),
+                                          shape.block_size) for m in range(shape.n_rows)])
+
+
+def small_cfg(name, **kw):
+    return CONFIGS[name].with_(**kw)
+
+
+# ----------------------------------------------------------------------- top-k
+
+TOPK_CASES = [
+    # (label, batch, seq, block, q_tile, top_k, kind)
+    ("tiny", 1, 1024, 64, 64, 4, "normal"),
+    ("ties", 1, 4096, 64, 64, 6, "ties"),
+    ("mixed_ragged", 2, 5000, 128, 64, 16, "mixed"),
+    ("k1", 1, 2048, 128, 64, 1, "normal"),
+    ("k_exceeds_candidates", 1, 3000, 64, 32, 40, "mixed"),
+    ("p32k", 1, 32768, 128, 64, 16, "mixed"),
+    ("p128k", 1, 131072, 128, 64, 32, "normal"),
+    ("q_tile1", 1, 700, 16, 1, 5, "ties"),
+]
+
+
+@pytest.mark.parametrize("case", TOPK_CASES, ids=[c[0] for c in TOPK_CASES])
+def test_topk_bit_exact(case):
+    label, B, T, bs, qt, k, kind = case
+    seed = TOPK_CASES.index(case)
+    shape = _lib.make_shape(B, T, T, 4 * 4, 4, 64, 64, bs, k, qt, "bf16")
+    sc = random_block_scores((B, 4, shape.n_rows, shape.n_blocks), seed=seed,
+                             kind=kind)
+    sel = torch.full((B, 4, shape.n_rows, k), -7, dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk(shape, torch.from_numpy(sc).to(DEV), sel)
+    torch.cuda.synchronize()
+    ref = oracle.block_topk_prefill(sc, T, qt, bs, k)
+    got = sel.cpu().numpy()
+    bad = np.argwhere(np.any(got != ref, axis=-1))
+    assert bad.size == 0, f"{len(bad)} rows differ, e.g. {bad[:2].tolist()}: " \
+        f"{got[tuple(bad[0])]} vs {ref[tuple(bad[0])]}"
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+def test_topk_decode_1m_bit_exact(kind):
+    B, L, bs, k = 8, 1 << 20, 128, 64
+    shape = _lib.make_shape(B, 1, L, 64, 4, 128, 128, bs, k, 1, "bf16")
+    sc = random_block_scores((B, 4, 1, shape.n_blocks), seed=5, kind=kind)
+    sel = torch.empty((B, 4, 1, k), dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk(shape, torch.from_numpy(sc).to(DEV), sel)
+    ref = oracle.block_topk_decode(sc, L, bs, k)
+    assert np.array_equal(sel.cpu().numpy(), ref)
+
+
+def test_topk_1m_prefill_rows_bit_exact():
+    """Rows of a 1M prefill (up to 8192 candidates each), sampled for the oracle."""
+    T, bs, qt, k = 1 << 20, 128, 128, 64
+    shape = _lib.make_shape(1, T, T, 64, 4, 128, 128, bs, k, qt, "bf16")
+    sc = random_block_scores((1, 4, shape.n_rows, shape.n_blocks), seed=9, kind="mixed")
+    sel = torch.empty((1, 4, shape.n_rows, k), dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk(shape, torch.from_numpy(sc).to(DEV), sel)
+    got = sel.cpu().numpy()
+    rows = sample_tiles(shape.n_rows, n_random=12, seed=3)
+    ref = oracle.block_topk_prefill(sc[:, :, rows], T, qt, bs, k, tiles=rows)
+    assert np.array_equal(got[:, :, rows], ref)
+
+
+# -------------------------------------------------------------- index scores
+
+def _index_case(cfg, tiles=None):
+    x = make_inputs(cfg, device=DEV)
+    shape = _lib.shape_from_config(cfg)
+    scores = torch.empty((cfg.batch, cfg.n_heads_kv, shape.n_rows, shape.n_blocks),
+                         dtype=torch.float32, device=DEV)
+    _lib.msa_index_scores(shape, x["idx_q"], x["idx_k"], scores)
+    torch.cuda.synchronize()
+    if cfg.mode == "decode":
+        ref = oracle.index_block_scores_decode(x["idx_q"], x["idx_k"], cfg.block_size)
+        return to_np(scores), ref
+    ref = oracle.index_block_scores_prefill(x["idx_q"], x["idx_k"], cfg.block_size, cfg.q_tile,
+                                            tiles=tiles)
+    got = to_np(scores)
+    return (got if tiles is None else got[:, :, tiles]), ref
+
+
+INDEX_CASES = {
+    "tiny_f32": lambda: small_cfg("tiny"),
+    "f32_ragged_qt16": lambda: small_cfg("tiny", seq=1000, q_tile=16, block_size=32),
+    "bf16_ragged_1000": lambda: small_cfg("p32k", seq=1000, n_plants=3),
+    "bf16_4096_d64": lambda: small_cfg("p32k", seq=4096, index_dim=64, block_size=64),
+    "bf16_8192": lambda: small_cfg("p32k", seq=8192, n_plants=5),
+    "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, n_plants=4),
+    "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", index_dim=64,
+                                    n_plants=2),
+}
+
+
+@pytest.mark.parametrize("name", list(INDEX_CASES))
+def test_index_scores(name):
+    got, ref = _index_case(INDEX_CASES[name]())
+    check_scores(got, ref, name)
+
+
+def test_index_scores_p32k_sampled():
+    cfg = CONFIGS["p32k"]
+    tiles = sample_tiles(cfg.n_tiles, seed=1)
+    got, ref = _index_case(cfg, tiles)
+    check_scores(got, ref, "p32k")
+
+
+def test_index_scores_d1m_full():
+    got, ref = _index_case(CONFIGS["d1m"])
+    check_scores(got, ref, "d1m")
+
+
+# ----------------------------------------------------------- sparse attention
+
+def _attn_case(cfg, sel_seed=0, tiles=None):
+    x = make_inputs(cfg, device=DEV)
+    shape = _lib.shape_from_config(cfg)
+    ncand = cur_blocks(shape) + 1
+    sel_np = random_selection(np.broadcast_to(ncand, (cfg.batch, cfg.n_heads_kv, len(ncand))),
+                              cfg.top_k, sel_seed)
+    sel = torch.from_numpy(sel_np).to(DEV)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((cfg.batch, cfg.n_heads_q, cfg.seq_q), dtype=torch.float32, device=DEV)
+    if cfg.mode == "decode":
+        nbytes = _lib.msa_workspace_bytes(shape, 1)
+        ws = torch.empty(nbytes // 4 + 4, dtype=torch.float32, device=DEV)
+        _lib.msa_sparse_decode(shape, x["q"], x["k"], x["v"], sel, out, lse, ws)
+        torch.cuda.synchronize()
+        ref_o, ref_l = oracle.sparse_attention(x["q"], x["k"], x["v"], sel_np, cfg.block_size, 1,
+                                               None, cfg.seq - 1)
+        return to_np(out), to_np(lse), ref_o, ref_l
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.sparse_attention(x["q"], x["k"], x["v"], sel_np, cfg.block_size,
+                                           cfg.q_tile, None, 0, tiles)
+    got_o, got_l = to_np(out), to_np(lse)
+    if tiles is not None:
+        rows = np.concatenate([np.arange(m * cfg.q_tile, min(cfg.seq, (m + 1) * cfg.q_tile))
+                               for m in tiles])
+        got_o, got_l = got_o[:, rows], got_l[:, :, rows]
+    return got_o, got_l, ref_o, ref_l
+
+
+ATTN_CASES = {
+    "tiny_f32": lambda: small_cfg("tiny"),
+    "f32_ragged": lambda: small_cfg("tiny", seq=1000, q_tile=16, block_size=32, top_k=5),
+    "bf16_ragged_1000": lambda: small_cfg("p32k", seq=1000, top_k=4, n_plants=3),
+    "bf16_d64_g16": lambda: small_cfg("p32k", seq=2048, head_dim=64, n_heads_q=64, top_k=6),
+    "bf16_4096_k16": lambda: small_cfg("p32k", seq=4096),
+    "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, top_k=8, n_plants=4),
+    "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", top_k=5,
+                                    head_dim=64, n_plants=2),
+    "decode_short_cache": lambda: small_cfg("d1m", batch=2, seq=200, top_k=64, n_plants=0),
+}
+
+
+@pytest.mark.parametrize("name", list(ATTN_CASES))
+def test_sparse_attention(name):
+    cfg = ATTN_CASES[name]()
+    got_o, got_l, ref_o, ref_l = _attn_case(cfg)
+    check_out(got_o, ref_o, cfg.dtype, name)
+    check_lse(got_l, ref_l, cfg.dtype, name)
+
+
+def test_sparse_prefill_p32k_sampled():
+    cfg = CONFIGS["p32k"]
+    tiles = sample_tiles(cfg.n_tiles, seed=2)
+    got_o, got_l, ref_o, ref_l = _attn_case(cfg, tiles=tiles)
+    check_out(got_o, ref_o, "bf16", "p32k")
+    check_lse(got_l, ref_l, "bf16", "p32k")
+
+
+def test_sparse_decode_d1m_full():
+    cfg = CONFIGS["d1m"]
+    got_o, got_l, ref_o, ref_l = _attn_case(cfg)
+    check_out(got_o, ref_o, "bf16", "d1m")
+    check_lse(got_l, ref_l, "bf16", "d1m")
+
+
+def test_empty_selection_rows():
+    """Rows whose list is all -1 attend to nothing: out 0, lse -inf."""
+    cfg = small_cfg("p32k", seq=512, top_k=3)
+    x = make_inputs(cfg, device=DEV)
+    shape = _lib.shape_from_config(cfg)
+    sel = torch.full((1, 4, shape.n_rows, 3), -1, dtype=torch.int32, device=DEV)
+    sel[:, :2, :, 0] = 0                       # heads 0-1 see block 0, heads 2-3 see nothing
+    out = torch.full_like(x["q"], 7.0)
+    lse = torch.zeros((1, cfg.n_heads_q, cfg.seq), dtype=torch.float32, device=DEV)
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    ref_o, ref_l = oracle.sparse_attention(x["q"], x["k"], x["v"], sel.cpu().numpy(),
+                                           cfg.block_size, cfg.q_tile)
+    check_out(out, ref_o, "bf16")
+    check_lse(lse, ref_l, "bf16")
+    assert torch.all(out[:, :, 16:] == 0)
+
+
+# ------------------------------------------------------------- whole pipeline
+
+def _pipeline(cfg, tiles=None):
+    x = make_inputs(cfg, device=DEV)
+    shape = _lib.shape_from_config(cfg)
+    if cfg.mode == "decode":
+        bufs = alloc_decode_outputs(shape, DEV, x["q"].dtype)
+        run_decode(shape, x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"], bufs)
+        torch.cuda.synchronize()
+        sc, sel, o, l = oracle.msa_decode(x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"],
+                                          cfg.block_size, cfg.top_k)
+        rows = [0]
+    else:
+        bufs = alloc_prefill_outputs(shape, DEV, x["q"].dtype)
+        run_prefill(shape, x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"], bufs)
+        torch.cuda.synchronize()
+        sc, sel, o, l = oracle.msa_prefill(x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"],
+                                           cfg.block_size, cfg.q_tile, cfg.top_k, tiles=tiles)
+        rows = list(range(shape.n_rows)) if tiles is None else tiles
+    g_sc, g_sel = to_np(bufs["scores"])[:, :, rows], to_np(bufs["sel"])[:, :, rows]
+    check_scores(g_sc, sc, cfg.name)
+    cb = np.broadcast_to(cur_blocks(shape)[rows], g_sel.shape[:-1])
+    agree = check_selection_valid(g_sel, sel, sc, cb, cfg.name)
+    # attention parity on the rows whose selection matches the oracle's
+    g_o, g_l = to_np(bufs["out"]), to_np(bufs["lse"])
+    qt = cfg.q_tile
+    for i, m in enumerate(rows):
+        t = np.arange(m * qt, min(cfg.seq_q, (m + 1) * qt))
+        r = np.arange(i * qt, i * qt + len(t))
+        for b in range(cfg.batch):
+            for g in range(cfg.n_heads_kv):
+                if not np.array_equal(g_sel[b, g, i], sel[b, g, i]):
+                    continue
+                hs = np.arange(g * cfg.group, (g + 1) * cfg.group)
+                check_out(g_o[b][np.ix_(t, hs)], o[b][np.ix_(r, hs)], cfg.dtype, cfg.name)
+                check_lse(g_l[b][np.ix_(hs, t)], l[b][np.ix_(hs, r)], cfg.dtype, cfg.name)
+    return agree
+
+
+def test_pipeline_tiny():
+    assert _pipeline(CONFIGS["tiny"]) >= 0.95
+
+
+def test_pipeline_tiny_scaled_plants_selected():
+    cfg = CONFIGS["tiny"]
+    x = make_inputs(cfg, device=DEV, input_scale=cfg.head_dim ** -0.5, plant_alpha=3.0)
+    shape = _lib.shape_from_config(cfg)
+    bufs = alloc_prefill_outputs(shape, DEV, x["q"].dtype)
+    run_prefill(shape, x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"], bufs)
+    sel = to_np(bufs["sel"])
+    for g in range(4):
+        for m in range(shape.n_rows):
+            cur = cur_blocks(shape)[m]
+            for p in x["plants"][0, g]:
+                if p < cur:
+                    assert p in sel[0, g, m]
+    # heads disagree somewhere: selections are per KV head
+    assert any(len({tuple(sel[0, g, m]) for g in range(4)}) > 1 for m in range(shape.n_rows))
+
+
+def test_pipeline_bf16_small():
+    assert _pipeline(small_cfg("p32k", seq=3000, n_plants=6)) >= 0.9
+
+
+def test_pipeline_p32k_sampled():
+    cfg = CONFIGS["p32k"]
+    assert _pipeline(cfg, tiles=sample_tiles(cfg.n_tiles, seed=4)) >= 0.9
+
+
+def test_pipeline_d1m():
+    assert _pipeline(CONFIGS["d1m"]) >= 0.9

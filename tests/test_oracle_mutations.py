@@ -23,14 +23,14 @@ def _fresh_oracle():
 def _mut_strict_mask(o):
     base = o.index_logits
 
-    def index_logits(idx_q_rows, idx_k, index_scale, q_pos):
-        return base(idx_q_rows, idx_k, index_scale, np.asarray(q_pos) - 1)  # drops j == t
+    def index_logits(idx_q_rows, idx_k, index_scale, q_pos, key_pos0=0):
+        return base(idx_q_rows, idx_k, index_scale, np.asarray(q_pos) - 1, key_pos0)  # j < t
     o.index_logits = index_logits
 
 
 def _mut_no_index_scale(o):
     base = o.index_logits
-    o.index_logits = lambda qr, kk, sc, pos: base(qr, kk, 1.0, pos)
+    o.index_logits = lambda qr, kk, sc, pos, key_pos0=0: base(qr, kk, 1.0, pos, key_pos0)
 
 
 def _mut_mean_pool(o):
@@ -111,11 +111,11 @@ def _mut_strided_groups(o):
 
 def _mut_transposed_index(o):
     # the index key of token j dotted with the index query of head g at token j's slot
-    def index_logits(idx_q_rows, idx_k, index_scale, q_pos):
+    def index_logits(idx_q_rows, idx_k, index_scale, q_pos, key_pos0=0):
         qr = np.asarray(idx_q_rows, dtype=np.float64)
         kk = np.asarray(idx_k, dtype=np.float64)
         s = index_scale * np.einsum("ngc,jc->gnj", qr[:, ::-1, :], kk)
-        j = np.arange(kk.shape[0])
+        j = key_pos0 + np.arange(kk.shape[0])
         vis = j[None, :] <= np.asarray(q_pos)[:, None]
         return np.where(vis[None], s, -np.inf)
     o.index_logits = index_logits
