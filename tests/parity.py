@@ -42,7 +42,7 @@ def check_scores(gpu, ref, what="scores"):
         f"{np.argwhere(g_inf != r_inf)[:5].tolist()}"
     assert not np.isnan(gpu).any(), f"{what}: NaN"
     fin = ~r_inf
-    err = np.abs(gpu - ref)
+    err = np.where(fin, np.abs(np.where(fin, gpu, 0.0) - np.where(fin, ref, 0.0)), 0.0)
     bound = score_bound(ref)
     bad = fin & (err > bound)
     assert not bad.any(), f"{what}: {bad.sum()} entries out of tolerance, worst " \
