@@ -43,6 +43,7 @@ SIGNATURES = {
     "msa_block_topk": (_i32, [_SHAPE_P, _vp, _vp, _vp]),
     "msa_sparse_prefill": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "msa_sparse_decode_static": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "msa_workspace_bytes": (_sz, [_SHAPE_P, ctypes.c_int]),
     "msa_get_device_status": (_i32, [_vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
@@ -153,6 +154,15 @@ def msa_sparse_decode(shape: MsaShape, q, k_cache, v_cache, sel, out, lse=None, 
     _check(load().msa_sparse_decode(ctypes.byref(shape), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                     _ptr(sel), _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                     _stream(stream)), "msa_sparse_decode")
+
+
+def msa_sparse_decode_static(shape: MsaShape, q, k_cache, v_cache, sel, out, lse=None,
+                             stream=None):
+    """msa_sparse_decode without a caller workspace: for callers that cannot allocate
+    device memory where decode runs, the library's own static device scratch is used."""
+    _check(load().msa_sparse_decode_static(ctypes.byref(shape), _ptr(q), _ptr(k_cache),
+                                           _ptr(v_cache), _ptr(sel), _ptr(out), _ptr(lse),
+                                           _stream(stream)), "msa_sparse_decode_static")
 
 
 def msa_workspace_bytes(shape: MsaShape, which: int) -> int:

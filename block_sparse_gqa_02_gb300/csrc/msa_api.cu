@@ -237,3 +237,77 @@ const char* msa_last_error(void) { return g_last_error; }
 int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
 
 }  // extern "C"
+
+// -----------------------------------------------------------------------------------------
+// Decode with library-held scratch, for callers that cannot allocate device memory where
+// decode runs (for example a plugin whose host framework owns every device allocation and
+// gives it no allocator, or a serving loop that must not allocate after start-up because
+// cudaMalloc can stall the device and can fail under memory pressure).  The split-KV
+// partial results go to a fixed array in device memory instead of a caller workspace.
+// -----------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace msa {
+namespace {
+
+// Largest split-KV scratch this entry point serves.  Every GPU that loads the library
+// holds this much device memory until the process exits.
+constexpr size_t kStaticScratchBytes = MSA_STATIC_DECODE_SCRATCH_BYTES;
+static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.  In host code the array's
+// name only stands in for the symbol, so the address is looked up once per device (with
+// that device current) and cached.
+cudaError_t static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace msa
+
+extern "C" msa_status msa_sparse_decode_static(const msa_shape* shape, const void* q,
+                                               const void* k_cache, const void* v_cache,
+                                               const int32_t* sel, void* out, float* lse,
+                                               void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  if (!d.decode) return fail(MSA_ERR_INVALID_ARG, "msa_sparse_decode_static needs seq_q == q_tile == 1");
+  if (d.G > 64) return fail(MSA_ERR_UNSUPPORTED, "decode needs n_heads_q / n_heads_kv <= 64");
+  MSA_TRY(check_ptr(q, "q"));
+  MSA_TRY(check_ptr(k_cache, "k_cache"));
+  MSA_TRY(check_ptr(v_cache, "v_cache"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  MSA_TRY(check_ptr(out, "out"));
+  MSA_TRY(check_ptr(lse, "lse", true));
+  const size_t need = decode_workspace_bytes(d);
+  if (need > kStaticScratchBytes)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "this shape needs %zu bytes of decode scratch; the library's static array "
+                "holds %zu (use msa_sparse_decode with a caller workspace)",
+                need, kStaticScratchBytes);
+  void* ws = nullptr;
+  cudaError_t e = static_scratch_address(&ws);
+  if (e != cudaSuccess) return cuda_fail(e, "msa_sparse_decode_static scratch address");
+  // Every partial slot the merge reads is written by this call first, so the array's
+  // previous contents never matter and nothing needs clearing.
+  e = launch_sparse_decode(d, q, k_cache, v_cache, sel, out, lse, static_cast<float*>(ws),
+                           (cudaStream_t)stream);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode_static launch");
+}

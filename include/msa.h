@@ -116,6 +116,29 @@ msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* 
                              const void* v_cache, const int32_t* sel, void* out, float* lse,
                              void* workspace, size_t ws_bytes, void* stream);
 
+/* Decode for callers that cannot allocate device memory.  Some callers have no way to
+ * call cudaMalloc where decode runs: a plugin whose host framework owns every device
+ * allocation and hands it no allocator, or a serving loop that must not allocate after
+ * start-up because cudaMalloc can stall the device and can fail under memory pressure.
+ * This entry point computes exactly what msa_sparse_decode computes, with the same
+ * arguments minus the workspace: the split-KV partial results go to a scratch array the
+ * library keeps in device memory (MSA_STATIC_DECODE_SCRATCH_BYTES, held on every GPU that
+ * loads the library until the process exits).  The talk pages have no counterpart to it.
+ *   - A shape whose scratch (msa_workspace_bytes(shape, 1)) exceeds the array is rejected
+ *     with MSA_ERR_UNSUPPORTED before anything runs; msa_last_error() names both sizes.
+ *   - The first call on each device looks up the array's device address with that device
+ *     current (cudaGetSymbolAddress) and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device uses the same array.  Calls that overlap on the GPU (other
+ *     streams, other host threads) race on it and corrupt each other's results: serialise
+ *     them.  Each call writes every scratch entry it reads, so leftovers of earlier calls do
+ *     not matter and nothing needs clearing.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine. */
+#define MSA_STATIC_DECODE_SCRATCH_BYTES (8u << 20)
+msa_status msa_sparse_decode_static(const msa_shape* shape, const void* q, const void* k_cache,
+                                    const void* v_cache, const int32_t* sel, void* out,
+                                    float* lse, void* stream);
+
 /* Scratch bytes msa_sparse_prefill (which = 0) or msa_sparse_decode (which = 1) needs for
  * this shape; 0 when none.  Returns 0 for an invalid shape. */
 size_t msa_workspace_bytes(const msa_shape* shape, int which);
