@@ -8,6 +8,7 @@
 // the tensor-core kernel does not cover, and the decode scan, which streams the index
 // key cache once from HBM.
 #include "common.cuh"
+#include "index_tc.cuh"
 
 namespace msa {
 
@@ -181,8 +182,11 @@ static cudaError_t dispatch_dim(const Dims& p, const void* iq, const void* ik, f
 
 cudaError_t launch_index_scores(const Dims& p, const void* idx_q, const void* idx_k,
                                 float* scores, cudaStream_t st, int* dev_status) {
-  (void)dev_status;
-  if (p.dtype == 1) return dispatch_dim<__nv_bfloat16>(p, idx_q, idx_k, scores, st);
+  if (p.dtype == 1) {
+    if (index_tc_supported(p))
+      return launch_index_scores_tc(p, idx_q, idx_k, scores, st, dev_status);
+    return dispatch_dim<__nv_bfloat16>(p, idx_q, idx_k, scores, st);
+  }
   return dispatch_dim<float>(p, idx_q, idx_k, scores, st);
 }
 
