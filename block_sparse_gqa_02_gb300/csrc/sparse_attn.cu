@@ -7,6 +7,7 @@
 // This file holds the CUDA-core kernels: prefill for fp32 and for shapes the tensor-core
 // kernel does not cover, and the split-KV decode with its log-sum-exp merge.
 #include "common.cuh"
+#include "sparse_prefill_tc.cuh"
 
 namespace msa {
 
@@ -264,7 +265,8 @@ size_t decode_workspace_bytes(const Dims& p) {
 cudaError_t launch_sparse_prefill(const Dims& p, const void* q, const void* k, const void* v,
                                   const int32_t* sel, void* out, float* lse, cudaStream_t st,
                                   int* dev_status) {
-  (void)dev_status;
+  if (p.dtype == 1 && sparse_prefill_tc_supported(p))
+    return launch_sparse_prefill_tc(p, q, k, v, sel, out, lse, st, dev_status);
   if (p.dtype == 1)
     return p.d == 128 ? prefill_simt<__nv_bfloat16, 128>(p, q, k, v, sel, out, lse, st)
                       : prefill_simt<__nv_bfloat16, 64>(p, q, k, v, sel, out, lse, st);

@@ -1,0 +1,425 @@
+// Main branch of MSA, prefill, on the tcgen05 tensor cores (bf16 inputs, fp32 softmax and
+// accumulation): exact attention of every query head over the blocks its KV head selected
+// ("How MiniMax M3 was built", aietalks.com, section "MSA uses a lightweight index branch
+// before sparse attention"; MiniMax稀疏注意力 topic page, summary: exact attention on the
+// selected blocks only).  The G query heads of a KV group share its selection, so one CTA
+// stacks (token, head) rows of one 64-query tile and streams only the selected 128-key
+// blocks of that KV head -- each block a contiguous 32 KiB run of the head-major K/V layout
+// (the pages' point about contiguous per-head reads for GQA).
+//
+// CTA = 256 rows of one (sequence, KV head, 64-query tile): two 128-row Q tiles that
+// ping-pong on the tensor core (while one tile's softmax runs, the other tile's MMAs do).
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P (bf16) is
+// written over the first 64 columns of S and read by the P.V MMA straight from TMEM.
+// Warps: 0-3 softmax + epilogue of Q tile 0, 4-7 of Q tile 1, 8 TMA producer, 9 MMA issuer.
+// Online softmax in the log2 domain with conditional rescaling: the running max used for
+// the exponent only moves when a block raises the row max by more than 8 (a factor 256),
+// so the O accumulator is rarely rescaled.  Every wait is bounded.
+#include "common.cuh"
+#include "ptx.cuh"
+#include "sparse_prefill_tc.cuh"
+#include "tma_host.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBk = 128;
+constexpr int kQt = 64;
+constexpr int kTileRows = 128;
+constexpr int kRowBytes = 128;
+constexpr int kTileBytes = 2 * kTileRows * kRowBytes;   // [2 chunks][128 rows][128 B] = 32 KiB
+constexpr int kKStages = 2;
+constexpr int kVStages = 2;
+constexpr int kMaxSel = 256;
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, kBk, 0, 0);
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, kD, 0, 1);
+constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct __align__(1024) Smem {
+  uint8_t q[2][kTileBytes];
+  uint8_t k[kKStages][kTileBytes];
+  uint8_t v[kVStages][kTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t v_full[kVStages], v_empty[kVStages];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_full[2];
+  int blocks[kMaxSel];
+  int n_sel;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void raise_abort(Smem& s, int* status, int code) {
+  s.abort = 1;
+  if (status) atomicExch(status, code);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const int32_t* __restrict__ sel, __nv_bfloat16* __restrict__ out,
+                         float* __restrict__ lse, Dims p, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                     ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = blockIdx.x;                   // which 256 rows of the tile's 64*G rows
+  const int m = p.nR - 1 - blockIdx.y;           // heaviest tiles first
+  const int bg = blockIdx.z, b = bg / p.Hkv, g = bg % p.Hkv;
+  const int G = p.G;
+  const int tok_per_tile = kTileRows / G;        // tokens in one 128-row Q tile
+  const volatile int* abort = &s.abort;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&s.q_full, 1);
+    for (int i = 0; i < kKStages; ++i) {
+      ptx::mbar_init(&s.k_full[i], 1);
+      ptx::mbar_init(&s.k_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      ptx::mbar_init(&s.v_full[i], 1);
+      ptx::mbar_init(&s.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.s_full[i], 1);
+      ptx::mbar_init(&s.p_full[i], 4);
+      ptx::mbar_init(&s.pv_done[i], 1);
+      ptx::mbar_init(&s.o_full[i], 1);
+    }
+    s.abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&s.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 1) {
+    // compact this row's selection (entries < 0 or >= nB are skipped), keeping its order
+    const int32_t* srow = sel + ((size_t)bg * p.nR + m) * p.k;
+    int n = 0;
+    for (int i0 = 0; i0 < p.k; i0 += 32) {
+      const int i = i0 + lane;
+      const int blk = i < p.k ? srow[i] : -1;
+      const bool ok = blk >= 0 && blk < p.nB;
+      const unsigned mask = __ballot_sync(0xffffffffu, ok);
+      if (ok) s.blocks[n + __popc(mask & ((1u << lane) - 1))] = blk;
+      n += __popc(mask);
+    }
+    if (lane == 0) s.n_sel = n;
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+  const int n_sel = s.n_sel;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------- TMA producer
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    if (lane == 0 && n_sel > 0) {
+      ptx::tma_prefetch_desc(&tm_q);
+      ptx::tma_prefetch_desc(&tm_k);
+      ptx::tma_prefetch_desc(&tm_v);
+      ptx::mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
+      for (int i = 0; i < 2; ++i) {
+        const int t0 = m * kQt + (part * 2 + i) * tok_per_tile;
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_4d(s.q[i] + kc * kTileRows * kRowBytes, &tm_q, &s.q_full, kc * 64,
+                           g * G, t0, b);
+      }
+    }
+    for (int j = 0; j < n_sel; ++j) {
+      const int blk = s.blocks[j];
+      const int ks = j % kKStages, vs = j % kVStages;
+      if (!ptx::mbar_wait(&s.k_empty[ks], ((j / kKStages) & 1) ^ 1, abort)) { ok = false; break; }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_3d(s.k[ks] + kc * kBk * kRowBytes, &tm_k, &s.k_full[ks], kc * 64,
+                           blk * kBk, bg);
+      }
+      k_issued = j + 1;
+      if (!ptx::mbar_wait(&s.v_empty[vs], ((j / kVStages) & 1) ^ 1, abort)) { ok = false; break; }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&s.v_full[vs], kTileBytes);
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_3d(s.v[vs] + kc * kBk * kRowBytes, &tm_v, &s.v_full[vs], kc * 64,
+                           blk * kBk, bg);
+      }
+      v_issued = j + 1;
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(s, status, 0x201);
+    if (*abort && lane == 0 && n_sel > 0) {
+      ptx::mbar_wait_timed(&s.q_full, 0);
+      for (int j = k_issued > kKStages ? k_issued - kKStages : 0; j < k_issued; ++j)
+        ptx::mbar_wait_timed(&s.k_full[j % kKStages], (j / kKStages) & 1);
+      for (int j = v_issued > kVStages ? v_issued - kVStages : 0; j < v_issued; ++j)
+        ptx::mbar_wait_timed(&s.v_full[j % kVStages], (j / kVStages) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    // -------------------------------------------------------------- MMA issuer
+    bool ok = true;
+    bool issued_any = false;
+    const uint32_t q0 = ptx::smem_u32(s.q[0]), q1 = ptx::smem_u32(s.q[1]);
+    auto issue_qk = [&](int i, int j) {
+      const uint32_t qa = i == 0 ? q0 : q1;
+      const uint32_t kb = ptx::smem_u32(s.k[j % kKStages]);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * (kTileRows * kRowBytes) + (kk & 3) * 32;
+        ptx::umma_bf16_ss(tmem + i * 128, ptx::smem_desc_k_sw128(qa + off),
+                          ptx::smem_desc_k_sw128(kb + off), kIdescQK, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int i, int j) {
+      const uint32_t vb = ptx::smem_u32(s.v[j % kVStages]);
+#pragma unroll
+      for (int kk = 0; kk < kBk / 16; ++kk)
+        ptx::umma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                          ptx::smem_desc_mn_sw128(vb + kk * 16 * kRowBytes, kBk * kRowBytes, 1024),
+                          kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    if (n_sel > 0) {
+      ok = ptx::mbar_wait(&s.q_full, 0, abort) && ptx::mbar_wait(&s.k_full[0], 0, abort);
+      if (ok) {
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          issue_qk(0, 0);
+          ptx::umma_commit(&s.s_full[0]);
+          issue_qk(1, 0);
+          ptx::umma_commit(&s.s_full[1]);
+          ptx::umma_commit(&s.k_empty[0]);
+        }
+        issued_any = true;
+        __syncwarp();
+      }
+      // Q.K^T of the next block overwrites S/P of a Q tile, which the P.V of the previous
+      // block reads from TMEM: it is issued only after that P.V has completed.
+      for (int j = 0; ok && j < n_sel; ++j) {
+        const bool more = j + 1 < n_sel;
+        if (!ptx::mbar_wait(&s.v_full[j % kVStages], (j / kVStages) & 1, abort) ||
+            !ptx::mbar_wait(&s.p_full[0], j & 1, abort)) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          issue_pv(0, j);
+          ptx::umma_commit(&s.pv_done[0]);
+        }
+        __syncwarp();
+        if (more) {
+          if (!ptx::mbar_wait(&s.k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort) ||
+              !ptx::mbar_wait(&s.pv_done[0], j & 1, abort)) { ok = false; break; }
+          ptx::tc_fence_after_sync();
+          if (lane == 0) {
+            issue_qk(0, j + 1);
+            ptx::umma_commit(&s.s_full[0]);
+          }
+          __syncwarp();
+        }
+        if (!ptx::mbar_wait(&s.p_full[1], j & 1, abort)) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          issue_pv(1, j);
+          ptx::umma_commit(&s.pv_done[1]);
+          ptx::umma_commit(&s.v_empty[j % kVStages]);
+          if (!more) {
+            ptx::umma_commit(&s.o_full[0]);
+            ptx::umma_commit(&s.o_full[1]);
+          }
+        }
+        __syncwarp();
+        if (more) {
+          if (!ptx::mbar_wait(&s.pv_done[1], j & 1, abort)) { ok = false; break; }
+          ptx::tc_fence_after_sync();
+          if (lane == 0) {
+            issue_qk(1, j + 1);
+            ptx::umma_commit(&s.s_full[1]);
+            ptx::umma_commit(&s.k_empty[(j + 1) % kKStages]);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_abort(s, status, 0x202);
+    if (*abort && lane == 0 && issued_any) {
+      // drain: one more commit covers every MMA issued so far
+      ptx::umma_commit(&s.o_full[0]);
+      ptx::mbar_wait_timed(&s.o_full[0], 0);
+    }
+  } else {
+    // ------------------------------------------------ softmax + epilogue (warps 0-7)
+    const int i = warp >> 2, quad = warp & 3;
+    const int r = quad * 32 + lane;                          // row in this Q tile
+    const int R = (part * 2 + i) * kTileRows + r;            // row in the 64*G tile rows
+    const int t = m * kQt + R / G;
+    const int h = g * G + R % G;
+    const bool valid = t < p.Sq;
+    const float c1 = p.sm_scale * 1.4426950408889634f;       // to log2 units
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_addr = tmem + lane_off + i * 128;
+    const uint32_t o_addr = tmem + lane_off + 256 + i * 128;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_sel; ++j) {
+      const int blk = s.blocks[j];
+      if (!ptx::mbar_wait(&s.s_full[i], j & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) ptx::tmem_ld_x32(s_addr + c * 32, sv[c]);
+      ptx::tmem_ld_wait();
+      // keys j > t are masked; only blocks reaching past the tile's first token need it
+      const int lim = t - blk * kBk;                         // visible columns: c <= lim
+      const bool need_mask = lim < kBk - 1;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x = __uint_as_float(sv[c][e]);
+          if (need_mask && c * 32 + e > lim) {
+            x = -INFINITY;
+            sv[c][e] = __float_as_uint(x);
+          }
+          mx = fmaxf(mx, x);
+        }
+      const float mb = mx * c1;                              // block max, log2 units
+      if (mb > m_used + kRescaleThreshold) {
+        const float m_new = mb;
+        if (m_used != -INFINITY) {
+          const float alpha = ex2(m_used - m_new);
+          l *= alpha;
+          // P.V of the previous block is complete (it precedes this block's Q.K^T)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32(o_addr + c * 32, ov);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            ptx::tmem_st_x32(o_addr + c * 32, ov);
+          }
+          ptx::tmem_st_wait();
+        }
+        m_used = m_new;
+      }
+      const float m_eff = m_used == -INFINITY ? 0.f : m_used;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[c][e]), c1, -m_eff));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), c1, -m_eff));
+          ls[(e >> 1) & 3] += p0 + p1;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+        }
+        ptx::tmem_st_x16(s_addr + c * 16, pk);
+      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.p_full[i]);
+    }
+    if (!ok && lane == 0) raise_abort(s, status, 0x203);
+    // epilogue: O / l -> bf16 row of out, lse
+    bool have_o = ok && n_sel > 0;
+    if (have_o) {
+      if (!ptx::mbar_wait(&s.o_full[i], 0, abort)) {
+        have_o = false;
+        if (lane == 0) raise_abort(s, status, 0x204);
+      }
+    }
+    if (have_o) ptx::tc_fence_after_sync();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = out + (((size_t)b * p.Sq + t) * p.Hq + h) * kD;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t ov[32];
+      if (have_o) {
+        ptx::tmem_ld_x32(o_addr + c * 32, ov);
+        ptx::tmem_ld_wait();
+      }
+      if (valid) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2)
+          pk[e >> 1] = have_o ? pack_bf16x2(__uint_as_float(ov[e]) * inv,
+                                            __uint_as_float(ov[e + 1]) * inv)
+                              : 0u;
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
+      }
+    }
+    if (valid && lse)
+      lse[((size_t)b * p.Hq + h) * p.Sq + t] =
+          l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool sparse_prefill_tc_supported(const Dims& p) {
+  return p.dtype == 1 && !p.decode && p.d == kD && p.Bk == kBk && p.Qt == kQt &&
+         p.G >= 4 && p.G <= 128 && (kTileRows % p.G) == 0 && p.k <= kMaxSel;
+}
+
+cudaError_t launch_sparse_prefill_tc(const Dims& p, const void* q, const void* k, const void* v,
+                                     const int32_t* sel, void* out, float* lse, cudaStream_t st,
+                                     int* status) {
+  CUtensorMap tq, tk, tv;
+  // q [B, T, Hq, d] as (d, Hq, T, B); one box = 64 dims x G heads x (128 / G) tokens
+  const uint64_t qd[4] = {(uint64_t)kD, (uint64_t)p.Hq, (uint64_t)p.Sq, (uint64_t)p.B};
+  const uint64_t qs[3] = {(uint64_t)kD * 2, (uint64_t)p.Hq * kD * 2,
+                          (uint64_t)p.Sq * p.Hq * kD * 2};
+  const uint32_t qb[4] = {64, (uint32_t)p.G, (uint32_t)(kTileRows / p.G), 1};
+  // k, v [B, Hkv, Sk, d] as (d, Sk, B * Hkv); one box = 64 dims x 128 keys
+  const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)p.Sk, (uint64_t)p.B * p.Hkv};
+  const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)p.Sk * kD * 2};
+  const uint32_t kb[3] = {64, (uint32_t)kBk, 1};
+  cudaError_t e = make_tensor_map_bf16(&tq, q, 4, qd, qs, qb);
+  if (e == cudaSuccess) e = make_tensor_map_bf16(&tk, k, 3, kd, ks, kb);
+  if (e == cudaSuccess) e = make_tensor_map_bf16(&tv, v, 3, kd, ks, kb);
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(Smem) + 1024;
+  e = cudaFuncSetAttribute(sparse_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.Qt * p.G / (2 * kTileRows), p.nR, p.B * p.Hkv);
+  sparse_prefill_tc_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, sel, (__nv_bfloat16*)out,
+                                                         lse, p, status);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

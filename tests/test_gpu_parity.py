@@ -176,6 +176,9 @@ ATTN_CASES = {
     "bf16_ragged_1000": lambda: small_cfg("p32k", seq=1000, top_k=4, n_plants=3),
     "bf16_d64_g16": lambda: small_cfg("p32k", seq=2048, head_dim=64, n_heads_q=64, top_k=6),
     "bf16_4096_k16": lambda: small_cfg("p32k", seq=4096),
+    "bf16_g4_ragged": lambda: small_cfg("p32k", seq=2000, n_heads_q=16, top_k=7),
+    "bf16_g32": lambda: small_cfg("p32k", seq=1100, n_heads_q=128, top_k=3),
+    "bf16_g16_k1": lambda: small_cfg("p32k", seq=700, n_heads_q=64, top_k=1),
     "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, top_k=8, n_plants=4),
     "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", top_k=5,
                                     head_dim=64, n_plants=2),
