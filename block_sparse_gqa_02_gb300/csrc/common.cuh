@@ -67,7 +67,7 @@ cudaError_t launch_sparse_prefill(const Dims& p, const void* q, const void* k,
                                   cudaStream_t st, int* dev_status);
 cudaError_t launch_sparse_decode(const Dims& p, const void* q, const void* k, const void* v,
                                  const int32_t* sel, void* out, float* lse, float* ws,
-                                 cudaStream_t st);
+                                 cudaStream_t st, int* dev_status);
 
 // Decode split-KV: number of block groups each (sequence, KV head) is split into, and
 // the scratch it needs (partial outputs and partial log-sum-exps, fp32).

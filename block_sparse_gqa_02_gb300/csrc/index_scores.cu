@@ -8,6 +8,7 @@
 // the tensor-core kernel does not cover, and the decode scan, which streams the index
 // key cache once from HBM.
 #include "common.cuh"
+#include "index_scan_tc.cuh"
 #include "index_tc.cuh"
 
 namespace msa {
@@ -185,6 +186,8 @@ cudaError_t launch_index_scores(const Dims& p, const void* idx_q, const void* id
   if (p.dtype == 1) {
     if (index_tc_supported(p))
       return launch_index_scores_tc(p, idx_q, idx_k, scores, st, dev_status);
+    if (index_scan_tc_supported(p))
+      return launch_index_scan_tc(p, idx_q, idx_k, scores, st, dev_status);
     return dispatch_dim<__nv_bfloat16>(p, idx_q, idx_k, scores, st);
   }
   return dispatch_dim<float>(p, idx_q, idx_k, scores, st);

@@ -193,7 +193,8 @@ msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* 
     return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes is too small: need %zu", ws_bytes,
                 need);
   cudaError_t e = launch_sparse_decode(d, q, k_cache, v_cache, sel, out, lse,
-                                       static_cast<float*>(workspace), (cudaStream_t)stream);
+                                       static_cast<float*>(workspace), (cudaStream_t)stream,
+                                       status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode launch");
 }
 
@@ -308,6 +309,6 @@ extern "C" msa_status msa_sparse_decode_static(const msa_shape* shape, const voi
   // Every partial slot the merge reads is written by this call first, so the array's
   // previous contents never matter and nothing needs clearing.
   e = launch_sparse_decode(d, q, k_cache, v_cache, sel, out, lse, static_cast<float*>(ws),
-                           (cudaStream_t)stream);
+                           (cudaStream_t)stream, status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode_static launch");
 }

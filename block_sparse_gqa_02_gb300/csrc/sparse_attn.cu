@@ -7,6 +7,7 @@
 // This file holds the CUDA-core kernels: prefill for fp32 and for shapes the tensor-core
 // kernel does not cover, and the split-KV decode with its log-sum-exp merge.
 #include "common.cuh"
+#include "sparse_decode_mma.cuh"
 #include "sparse_prefill_tc.cuh"
 
 namespace msa {
@@ -226,21 +227,26 @@ cudaError_t prefill_simt(const Dims& p, const void* q, const void* k, const void
 }
 
 template <typename T, int D>
-cudaError_t decode_simt(const Dims& p, const void* q, const void* k, const void* v,
-                        const int32_t* sel, void* out, float* lse, float* ws, cudaStream_t st) {
+cudaError_t decode_split(const Dims& p, const void* q, const void* k, const void* v,
+                         const int32_t* sel, void* out, float* lse, float* ws, cudaStream_t st,
+                         int* dev_status) {
   const int n_split = decode_num_splits(p);
   const int per = (p.k + n_split - 1) / n_split;
   float* ws_o = ws;
   float* ws_l = ws + (size_t)p.B * p.Hq * n_split * D;
-  const size_t smem = 2 * (size_t)kKC * D * sizeof(float);
-  auto kern = sparse_decode_partial_simt<T, D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid(n_split, 1, p.B * p.Hkv);
-  kern<<<grid, kThreads, smem, st>>>((const T*)q, (const T*)k, (const T*)v, sel, ws_o, ws_l, p,
-                                     n_split, per);
-  e = cudaGetLastError();
+  cudaError_t e;
+  if (sparse_decode_mma_supported(p)) {
+    e = launch_sparse_decode_mma(p, q, k, v, sel, ws_o, ws_l, n_split, per, st, dev_status);
+  } else {
+    const size_t smem = 2 * (size_t)kKC * D * sizeof(float);
+    auto kern = sparse_decode_partial_simt<T, D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(n_split, 1, p.B * p.Hkv);
+    kern<<<grid, kThreads, smem, st>>>((const T*)q, (const T*)k, (const T*)v, sel, ws_o, ws_l,
+                                       p, n_split, per);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   decode_combine<T, D><<<p.B * p.Hq, D, 0, st>>>(ws_o, ws_l, (T*)out, lse, p, n_split);
   return cudaGetLastError();
@@ -276,12 +282,13 @@ cudaError_t launch_sparse_prefill(const Dims& p, const void* q, const void* k, c
 
 cudaError_t launch_sparse_decode(const Dims& p, const void* q, const void* k, const void* v,
                                  const int32_t* sel, void* out, float* lse, float* ws,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, int* dev_status) {
   if (p.dtype == 1)
-    return p.d == 128 ? decode_simt<__nv_bfloat16, 128>(p, q, k, v, sel, out, lse, ws, st)
-                      : decode_simt<__nv_bfloat16, 64>(p, q, k, v, sel, out, lse, ws, st);
-  return p.d == 128 ? decode_simt<float, 128>(p, q, k, v, sel, out, lse, ws, st)
-                    : decode_simt<float, 64>(p, q, k, v, sel, out, lse, ws, st);
+    return p.d == 128
+               ? decode_split<__nv_bfloat16, 128>(p, q, k, v, sel, out, lse, ws, st, dev_status)
+               : decode_split<__nv_bfloat16, 64>(p, q, k, v, sel, out, lse, ws, st, dev_status);
+  return p.d == 128 ? decode_split<float, 128>(p, q, k, v, sel, out, lse, ws, st, dev_status)
+                    : decode_split<float, 64>(p, q, k, v, sel, out, lse, ws, st, dev_status);
 }
 
 }  // namespace msa

@@ -116,6 +116,7 @@ INDEX_CASES = {
     "bf16_4096_d64": lambda: small_cfg("p32k", seq=4096, index_dim=64, block_size=64),
     "bf16_8192": lambda: small_cfg("p32k", seq=8192, n_plants=5),
     "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, n_plants=4),
+    "decode_tiny_cache": lambda: small_cfg("d1m", batch=3, seq=77, n_plants=0),
     "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", index_dim=64,
                                     n_plants=2),
 }
@@ -183,6 +184,10 @@ ATTN_CASES = {
     "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", top_k=5,
                                     head_dim=64, n_plants=2),
     "decode_short_cache": lambda: small_cfg("d1m", batch=2, seq=200, top_k=64, n_plants=0),
+    "decode_g8": lambda: small_cfg("d1m", batch=3, seq=9000, n_heads_q=32, top_k=12,
+                                   n_plants=4),
+    "decode_g4_k3": lambda: small_cfg("d1m", batch=5, seq=1000, n_heads_q=16, top_k=3,
+                                      n_plants=2),
 }
 
 
