@@ -73,10 +73,27 @@ def load_peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
+# ------------------------------------------------------------------- multi-rank
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest value any rank holds (each rank times its own replica; the job's time is
+    the slowest rank's).  A timing reduction only: no data of the path crosses ranks."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(units_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time (weak scaling)."""
+    return world * units_per_step * steps / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of the SM clock and throttle reasons while running."""
+    """nvidia-smi samples (every 50 ms) of the SM clock and throttle reasons while running."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -90,7 +107,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -212,6 +229,39 @@ def e2e_prefill(cfg, step, stream, n_steps):
             "steps": n_steps}, host
 
 
+def prefill_1m(args, device, stream, flush, tc_peak):
+    """The same prefill pass at 1M context (a secondary measurement, same method)."""
+    cfg = CONFIGS["p1m"]
+    step = Step(cfg, device)
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        step.run(stream, False)
+    torch.cuda.synchronize()
+    for _ in range(args.steps_1m):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        step.run(stream, True)
+    torch.cuda.synchronize()
+    _lib.msa_get_device_status(stream)
+    t = step.times_ms()
+    f_index, f_sparse, f_dense = prefill_flops(cfg)
+    ms = float(t[:, 0].mean())
+    k_idx, k_topk, k_attn = (float(t[:, i].mean()) for i in (1, 2, 3))
+    out = {"workload": f"{cfg.name}: {cfg.description}", "steps": args.steps_1m,
+           "tokens_per_s": cfg.seq * cfg.batch / (ms / 1e3), "ms_per_step": ms,
+           "kernels_ms": {"index_scores": k_idx, "block_topk": k_topk, "sparse_prefill": k_attn},
+           "index_tflops": f_index / (k_idx / 1e3) / 1e12,
+           "sparse_tflops": f_sparse / (k_attn / 1e3) / 1e12,
+           "index_frac": f_index / (k_idx / 1e3) / 1e12 / tc_peak,
+           "sparse_frac": f_sparse / (k_attn / 1e3) / 1e12 / tc_peak,
+           "msa_tflops_per_s": (f_index + f_sparse) / (ms / 1e3) / 1e12,
+           "dense_flops_avoided": f_dense - f_sparse}
+    del step
+    torch.cuda.empty_cache()
+    return out
+
+
 def cpu_baseline_prefill(cfg, host, budget_s=15.0, seed=0):
     """The oracle as it stands on the host cores, on uniformly sampled query tiles of the
     same prefill (all heads); tokens/s = q_tile * tiles / time, an unbiased estimate of
@@ -237,6 +287,9 @@ def run_ours(args, rank, world, device):
     _lib.load()
     pcfg = CONFIGS[args.prefill]
     dcfg = CONFIGS[args.decode]
+    if args.decode_len:
+        dcfg = dcfg.with_(seq=args.decode_len, name=f"{dcfg.name}-L{args.decode_len}",
+                          description=f"{dcfg.description} (cache length {args.decode_len})")
     stream = torch.cuda.Stream(device)
     pre = Step(pcfg, device)
     dec = Step(dcfg, device) if not args.no_decode else None
@@ -273,11 +326,7 @@ def run_ours(args, rank, world, device):
 
     pt = pre.times_ms()
     dt = dec.times_ms() if dec else None
-    pre_ms = float(pt[:, 0].sum())
-    if world > 1:
-        t = torch.tensor([pre_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        pre_ms = float(t.item())
+    pre_ms = max_over_ranks(float(pt[:, 0].sum()), world, device)
     if rank != 0:
         return None
 
@@ -287,7 +336,7 @@ def run_ours(args, rank, world, device):
     f_index, f_sparse, f_dense = prefill_flops(pcfg)
     k_idx, k_topk, k_attn = (float(pt[:, i].mean()) for i in (1, 2, 3))
     tokens = pcfg.seq * pcfg.batch
-    value = world * tokens * args.steps / (pre_ms / 1e3)
+    value = whole_job_throughput(tokens, args.steps, world, pre_ms)
     attn_tf = f_sparse / (k_attn / 1e3) / 1e12
     idx_tf = f_index / (k_idx / 1e3) / 1e12
     line = {
@@ -314,6 +363,8 @@ def run_ours(args, rank, world, device):
         "msa_prefill_tflops_per_s": (f_index + f_sparse) / (pre_ms / args.steps / 1e3) / 1e12,
         "clocks": clk,
         "gpu_launches": args.steps * (pre.kernels + (dec.kernels if dec else 0)),
+        "gpu_launches_note": "library kernels in the timed region of the headline steps "
+                             "(prefill 3 + decode 4 per step); the 1M prefill is timed apart",
         "wall_s_timed_region": wall,
     }
     if dec:
@@ -332,6 +383,8 @@ def run_ours(args, rank, world, device):
             "step_hbm_gbs": (b_scan + b_rest) / (d_total / 1e3) / 1e9,
             "dense_bytes_avoided": b_dense - (b_scan + b_rest),
         }
+    if not args.no_1m and pcfg.name != "p1m":
+        line["prefill_1m"] = prefill_1m(args, device, stream, flush, tc_peak)
     if not args.no_e2e:
         e2e, host = e2e_prefill(pcfg, pre, stream, max(2, min(args.steps, 5)))
         line["e2e"] = e2e
@@ -382,12 +435,17 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
     ap.add_argument("--prefill", default="p128k", choices=["p32k", "p128k", "p1m"])
     ap.add_argument("--decode", default="d1m", choices=["d1m"])
+    ap.add_argument("--decode-len", type=int, default=0,
+                    help="override the decode cache length (smaller cases for profiling)")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-1m", action="store_true",
+                    help="skip the secondary 1M-context prefill measurement")
+    ap.add_argument("--steps-1m", type=int, default=3)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
