@@ -16,8 +16,6 @@ namespace msa {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -26,7 +24,9 @@ __device__ __forceinline__ uint32_t order_key(float x) {
 }
 
 // Exclusive prefix sum of one value per thread over the CTA; also returns the total.
+template <int kThreads>
 __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_sums, int& total) {
+  constexpr int kWarps = kThreads / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -52,8 +52,10 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_sums, int& to
   return before;
 }
 
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __restrict__ scores,
                                                               int32_t* __restrict__ sel, Dims p) {
+  constexpr int kWarps = kThreads / 32;
   extern __shared__ uint32_t keys[];                        // [cb]
   __shared__ uint32_t hist[256];
   __shared__ int warp_sums[kWarps];
@@ -62,9 +64,15 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
 
   const int row = blockIdx.x;                               // (b * Hkv + g) * nR + m
   const int m = row % p.nR;
-  const int cb = row_last_pos(p, m) / p.Bk;
+  // ragged decode: the query of sequence b sits at its own cache length - 1
+  const int last = p.seq_lens ? seq_len_of(p, row / (p.Hkv * p.nR)) - 1 : row_last_pos(p, m);
   const float* srow = scores + (size_t)row * p.nB;
   int32_t* out = sel + (size_t)row * p.k;
+  if (last < 0) {                                           // empty sequence: nothing visible
+    for (int i = threadIdx.x; i < p.k; i += kThreads) out[i] = -1;
+    return;
+  }
+  const int cb = last / p.Bk;
 
   if (cb + 1 <= p.k) {                                      // every candidate fits
     for (int i = threadIdx.x; i < p.k; i += kThreads) out[i] = i <= cb ? i : -1;
@@ -133,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
   int n_eq = 0;
   for (int i = lo; i < hi; ++i) n_eq += keys[i] == tau;
   int total;
-  const int eq_before = cta_exclusive_scan(n_eq, warp_sums, total);
+  const int eq_before = cta_exclusive_scan<kThreads>(n_eq, warp_sums, total);
   int n_take = 0;
   {
     int rank = eq_before;
@@ -143,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
       else if (key == tau) n_take += (rank++ < take_eq);
     }
   }
-  const int pos0 = cta_exclusive_scan(n_take, warp_sums, total);
+  const int pos0 = cta_exclusive_scan<kThreads>(n_take, warp_sums, total);
   {
     int rank = eq_before, pos = pos0;
     for (int i = lo; i < hi; ++i) {
@@ -157,18 +165,25 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
 
 }  // namespace
 
-cudaError_t launch_block_topk(const Dims& p, const float* scores, int32_t* sel,
-                              cudaStream_t st) {
+template <int kThreads>
+static cudaError_t launch_rows(const Dims& p, const float* scores, int32_t* sel, cudaStream_t st) {
   const int rows = p.B * p.Hkv * p.nR;
-  if (rows == 0) return cudaSuccess;
   const size_t smem = (size_t)p.nB * sizeof(uint32_t);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(block_topk_kernel,
+    cudaError_t e = cudaFuncSetAttribute(block_topk_kernel<kThreads>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  block_topk_kernel<<<rows, kThreads, smem, st>>>(scores, sel, p);
+  block_topk_kernel<kThreads><<<rows, kThreads, smem, st>>>(scores, sel, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_block_topk(const Dims& p, const float* scores, int32_t* sel,
+                              cudaStream_t st) {
+  if (p.B * p.Hkv * p.nR == 0) return cudaSuccess;
+  // long rows (decode at 1M context: 8192 candidates) get more threads per row
+  if (p.nB > 2048) return launch_rows<1024>(p, scores, sel, st);
+  return launch_rows<256>(p, scores, sel, st);
 }
 
 }  // namespace msa

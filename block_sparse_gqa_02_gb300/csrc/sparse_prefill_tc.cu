@@ -62,6 +62,39 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Packed pairs of fp32 (one 64-bit register) for the paired FMA / ADD instructions.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo_f32(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return lo;
+}
+__device__ __forceinline__ float hi_f32(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return hi;
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -72,6 +105,8 @@ __device__ __forceinline__ void raise_abort(Smem& s, int* status, int code) {
   if (status) atomicExch(status, code);
 }
 
+// 10 warps: three of them share one SM sub-partition's 16K-entry register file, which caps
+// a thread at 168 registers.
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -136,7 +171,9 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ------------------------------------------------------------- TMA producer
     int k_issued = 0, v_issued = 0;
     bool ok = true;
-    if (lane == 0 && n_sel > 0) {
+    // test hook: issue nothing, so the consumers' bounded waits run out
+    const int n_load = p.inject == 1 ? 0 : n_sel;
+    if (lane == 0 && n_load > 0) {
       ptx::tma_prefetch_desc(&tm_q);
       ptx::tma_prefetch_desc(&tm_k);
       ptx::tma_prefetch_desc(&tm_v);
@@ -148,7 +185,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                            g * G, t0, b);
       }
     }
-    for (int j = 0; j < n_sel; ++j) {
+    for (int j = 0; j < n_load; ++j) {
       const int blk = s.blocks[j];
       const int ks = j % kKStages, vs = j % kVStages;
       if (!ptx::mbar_wait(&s.k_empty[ks], ((j / kKStages) & 1) ^ 1, abort)) { ok = false; break; }
@@ -170,7 +207,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(s, status, 0x201);
-    if (*abort && lane == 0 && n_sel > 0) {
+    if (*abort && lane == 0 && n_load > 0) {
       ptx::mbar_wait_timed(&s.q_full, 0);
       for (int j = k_issued > kKStages ? k_issued - kKStages : 0; j < k_issued; ++j)
         ptx::mbar_wait_timed(&s.k_full[j % kKStages], (j / kKStages) & 1);
@@ -288,56 +325,69 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
       for (int c = 0; c < 4; ++c) ptx::tmem_ld_x32(s_addr + c * 32, sv[c]);
       ptx::tmem_ld_wait();
-      // keys j > t are masked; only blocks reaching past the tile's first token need it
+      // keys j > t are masked; only a block reaching past this row's token needs it
       const int lim = t - blk * kBk;                         // visible columns: c <= lim
-      const bool need_mask = lim < kBk - 1;
       float mx = -INFINITY;
+      if (lim >= kBk - 1) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x = __uint_as_float(sv[c][e]);
-          if (need_mask && c * 32 + e > lim) {
-            x = -INFINITY;
+          for (int e = 0; e < 32; e += 2)
+            mx = max3(mx, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = c * 32 + e <= lim ? __uint_as_float(sv[c][e]) : -INFINITY;
             sv[c][e] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
           }
-          mx = fmaxf(mx, x);
-        }
+      }
       const float mb = mx * c1;                              // block max, log2 units
+      float alpha = 1.f;
+      bool rescale = false;
       if (mb > m_used + kRescaleThreshold) {
-        const float m_new = mb;
         if (m_used != -INFINITY) {
-          const float alpha = ex2(m_used - m_new);
+          alpha = ex2(m_used - mb);
+          rescale = true;
           l *= alpha;
-          // P.V of the previous block is complete (it precedes this block's Q.K^T)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            ptx::tmem_ld_x32(o_addr + c * 32, ov);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            ptx::tmem_st_x32(o_addr + c * 32, ov);
-          }
-          ptx::tmem_st_wait();
         }
-        m_used = m_new;
+        m_used = mb;
       }
       const float m_eff = m_used == -INFINITY ? 0.f : m_used;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s * c1 - m): pairs of columns through packed fp32 FMA / ADD
+      const uint64_t c1x2 = f32x2(c1, c1), negm = f32x2(-m_eff, -m_eff);
+      uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[c][e]), c1, -m_eff));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), c1, -m_eff));
-          ls[(e >> 1) & 3] += p0 + p1;
+          const uint64_t y = fma_f32x2(f32x2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])),
+                                       c1x2, negm);
+          const float p0 = ex2(lo_f32(y)), p1 = ex2(hi_f32(y));
+          const uint64_t pp = f32x2(p0, p1);
+          if ((e >> 1) & 1) acc1 = add_f32x2(acc1, pp); else acc0 = add_f32x2(acc0, pp);
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
         ptx::tmem_st_x16(s_addr + c * 16, pk);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      const uint64_t acc = add_f32x2(acc0, acc1);
+      l += lo_f32(acc) + hi_f32(acc);
+      if (rescale) {
+        // P.V of the previous block is complete (it precedes this block's Q.K^T); O is
+        // rescaled before this block's P is released to the MMA warp
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          ptx::tmem_ld_x32(o_addr + c * 32, ov);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          ptx::tmem_st_x32(o_addr + c * 32, ov);
+        }
+      }
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
       __syncwarp();
