@@ -44,11 +44,16 @@ SIGNATURES = {
     "msa_sparse_prefill": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode_static": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "msa_index_scores_paged": (_i32, [_SHAPE_P, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
+    "msa_block_topk_ragged": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp]),
+    "msa_sparse_decode_paged": (_i32, [_SHAPE_P, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _vp, _sz, _vp]),
     "msa_workspace_bytes": (_sz, [_SHAPE_P, ctypes.c_int]),
     "msa_get_device_status": (_i32, [_vp]),
     "msa_status_string": (ctypes.c_char_p, [_i32]),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_abi_version": (_i32, []),
+    "msa_debug_set_fault": (_i32, [_i32]),
 }
 
 _lock = threading.Lock()
@@ -165,6 +170,29 @@ def msa_sparse_decode_static(shape: MsaShape, q, k_cache, v_cache, sel, out, lse
                                            _stream(stream)), "msa_sparse_decode_static")
 
 
+def msa_index_scores_paged(shape: MsaShape, seq_lens, block_table, n_phys, idx_q, idx_k_pool,
+                           block_scores, stream=None):
+    _check(load().msa_index_scores_paged(ctypes.byref(shape), _ptr(seq_lens), _ptr(block_table),
+                                         int(n_phys), _ptr(idx_q), _ptr(idx_k_pool),
+                                         _ptr(block_scores), _stream(stream)),
+           "msa_index_scores_paged")
+
+
+def msa_block_topk_ragged(shape: MsaShape, seq_lens, block_scores, sel, stream=None):
+    _check(load().msa_block_topk_ragged(ctypes.byref(shape), _ptr(seq_lens), _ptr(block_scores),
+                                        _ptr(sel), _stream(stream)), "msa_block_topk_ragged")
+
+
+def msa_sparse_decode_paged(shape: MsaShape, seq_lens, block_table, n_phys, q, k_pool, v_pool,
+                            sel, out, lse=None, workspace=None, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().msa_sparse_decode_paged(ctypes.byref(shape), _ptr(seq_lens), _ptr(block_table),
+                                          int(n_phys), _ptr(q), _ptr(k_pool), _ptr(v_pool),
+                                          _ptr(sel), _ptr(out), _ptr(lse), _ptr(workspace),
+                                          ws_bytes, _stream(stream)), "msa_sparse_decode_paged")
+
+
 def msa_workspace_bytes(shape: MsaShape, which: int) -> int:
     return int(load().msa_workspace_bytes(ctypes.byref(shape), which))
 
@@ -175,3 +203,8 @@ def msa_get_device_status(stream=None):
 
 def msa_abi_version() -> int:
     return int(load().msa_abi_version())
+
+
+def msa_debug_set_fault(mode: int):
+    """Test hook: mode 1 makes tensor-core prefill launches time out (see include/msa.h)."""
+    _check(load().msa_debug_set_fault(mode), "msa_debug_set_fault")

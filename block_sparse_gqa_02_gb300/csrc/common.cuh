@@ -17,7 +17,20 @@ struct Dims {
   int decode;    // 1 when Sq == 1 and Qt == 1
   int dtype;     // 0 f32, 1 bf16
   float sm_scale, index_scale;
+  int inject;    // test hook: 1 = the tensor-core prefill producer issues no copies
+  // paged decode (all null / 0 for contiguous caches): per-sequence cache lengths [B],
+  // block table [B, nB] of physical block ids, and the number of physical blocks
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int n_phys;
 };
+
+// Cache length of sequence b (the decode query sits at position len - 1).
+__device__ __forceinline__ int seq_len_of(const Dims& p, int b) {
+  if (!p.seq_lens) return p.Sk;
+  const int L = p.seq_lens[b];
+  return L < 0 ? 0 : (L > p.Sk ? p.Sk : L);
+}
 
 // Position of the last query of selection row m; its block is the row's current block.
 __host__ __device__ inline int row_last_pos(const Dims& p, int m) {

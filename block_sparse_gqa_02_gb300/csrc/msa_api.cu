@@ -16,6 +16,7 @@ __device__ int g_device_status = 0;
 namespace {
 
 thread_local char g_last_error[512] = "";
+int g_fault_mode = 0;   // msa_debug_set_fault
 
 msa_status fail(msa_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 msa_status fail(msa_status st, const char* fmt, ...) {
@@ -97,6 +98,10 @@ msa_status make_dims(const msa_shape* s, Dims* d) {
   d->dtype = s->dtype;
   d->sm_scale = s->sm_scale > 0.f ? s->sm_scale : 1.f / sqrtf((float)s->head_dim);
   d->index_scale = s->index_scale > 0.f ? s->index_scale : 1.f / sqrtf((float)s->index_dim);
+  d->inject = g_fault_mode;
+  d->seq_lens = nullptr;
+  d->block_table = nullptr;
+  d->n_phys = 0;
   return MSA_OK;
 }
 
@@ -198,6 +203,84 @@ msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* 
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode launch");
 }
 
+// ------------------------------------------------------------- paged / ragged decode
+
+namespace {
+msa_status make_paged_dims(const msa_shape* shape, const int32_t* seq_lens,
+                           const int32_t* block_table, int32_t n_phys, Dims* d,
+                           bool need_table) {
+  MSA_TRY(make_dims(shape, d));
+  if (!d->decode) return fail(MSA_ERR_INVALID_ARG, "paged decode needs seq_q == q_tile == 1");
+  if (d->dtype != MSA_BF16 || d->d != 128 || d->dI != 128 || d->Bk != 128 || d->Hkv != 4 ||
+      d->G > 16)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "paged decode runs bf16, head_dim = index_dim = 128, block 128, 4 KV heads, "
+                "at most 16 query heads per KV head");
+  MSA_TRY(check_ptr(seq_lens, "seq_lens"));
+  if (need_table) {
+    MSA_TRY(check_ptr(block_table, "block_table"));
+    if (n_phys < 1) return fail(MSA_ERR_INVALID_ARG, "n_phys must be >= 1");
+  }
+  d->seq_lens = seq_lens;
+  d->block_table = need_table ? block_table : nullptr;
+  d->n_phys = need_table ? n_phys : 0;
+  return MSA_OK;
+}
+}  // namespace
+
+msa_status msa_index_scores_paged(const msa_shape* shape, const int32_t* seq_lens,
+                                  const int32_t* block_table, int32_t n_phys, const void* idx_q,
+                                  const void* idx_k_pool, float* block_scores, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_paged_dims(shape, seq_lens, block_table, n_phys, &d, true));
+  MSA_TRY(check_ptr(idx_q, "idx_q"));
+  MSA_TRY(check_ptr(idx_k_pool, "idx_k_pool"));
+  MSA_TRY(check_ptr(block_scores, "block_scores"));
+  cudaError_t e = launch_index_scores(d, idx_q, idx_k_pool, block_scores, (cudaStream_t)stream,
+                                      status_ptr());
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_scores_paged launch");
+}
+
+msa_status msa_block_topk_ragged(const msa_shape* shape, const int32_t* seq_lens,
+                                 const float* block_scores, int32_t* sel, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  if (!d.decode) return fail(MSA_ERR_INVALID_ARG, "ragged top-k needs seq_q == q_tile == 1");
+  MSA_TRY(check_ptr(seq_lens, "seq_lens"));
+  MSA_TRY(check_ptr(block_scores, "block_scores"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  d.seq_lens = seq_lens;
+  cudaError_t e = launch_block_topk(d, block_scores, sel, (cudaStream_t)stream);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_block_topk_ragged launch");
+}
+
+msa_status msa_sparse_decode_paged(const msa_shape* shape, const int32_t* seq_lens,
+                                   const int32_t* block_table, int32_t n_phys, const void* q,
+                                   const void* k_pool, const void* v_pool, const int32_t* sel,
+                                   void* out, float* lse, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_paged_dims(shape, seq_lens, block_table, n_phys, &d, true));
+  MSA_TRY(check_ptr(q, "q"));
+  MSA_TRY(check_ptr(k_pool, "k_pool"));
+  MSA_TRY(check_ptr(v_pool, "v_pool"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  MSA_TRY(check_ptr(out, "out"));
+  MSA_TRY(check_ptr(lse, "lse", true));
+  MSA_TRY(check_ptr(workspace, "workspace"));
+  const size_t need = decode_workspace_bytes(d);
+  if (ws_bytes < need)
+    return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes is too small: need %zu", ws_bytes,
+                need);
+  cudaError_t e = launch_sparse_decode(d, q, k_pool, v_pool, sel, out, lse,
+                                       static_cast<float*>(workspace), (cudaStream_t)stream,
+                                       status_ptr());
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode_paged launch");
+}
+
 size_t msa_workspace_bytes(const msa_shape* shape, int which) {
   Dims d;
   if (make_dims(shape, &d) != MSA_OK) return 0;
@@ -234,6 +317,12 @@ const char* msa_status_string(msa_status status) {
 }
 
 const char* msa_last_error(void) { return g_last_error; }
+
+msa_status msa_debug_set_fault(int32_t mode) {
+  if (mode != 0 && mode != 1) return fail(MSA_ERR_INVALID_ARG, "fault mode must be 0 or 1");
+  g_fault_mode = mode;
+  return MSA_OK;
+}
 
 int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
 

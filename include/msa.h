@@ -139,6 +139,34 @@ msa_status msa_sparse_decode_static(const msa_shape* shape, const void* q, const
                                     const void* v_cache, const int32_t* sel, void* out,
                                     float* lse, void* stream);
 
+/* Decode over a paged cache with a length per sequence (the serving form of decode).
+ * shape: a decode shape (seq_q = q_tile = 1) whose seq_k is the capacity of the block table
+ * (n_blocks = ceil(seq_k / block_size) entries per sequence); bf16, head_dim = index_dim =
+ * 128, block_size 128, 4 KV heads, at most 16 query heads per KV head.
+ *   seq_lens     int32 [batch], device: cache length L_b of sequence b, 1 <= L_b <= seq_k
+ *                (the new token, at position L_b - 1, is already in the cache; 0 means an
+ *                empty sequence: scores -inf, sel -1, out 0, lse -inf).
+ *   block_table  int32 [batch, n_blocks], device: physical block holding logical block j of
+ *                sequence b (entries past the sequence's last block are not read).
+ *   n_phys       number of physical blocks in the pools.
+ *   idx_k_pool   [n_phys, block_size, index_dim];  k_pool, v_pool [n_phys, n_heads_kv,
+ *                block_size, head_dim]: one physical block holds all KV heads' keys of 128
+ *                consecutive positions, each head's block contiguous.
+ * Semantics are those of the contiguous decode on each sequence's logical cache.  Entries
+ * of block_table outside [0, n_phys) read as zeros (no fault) and give meaningless output.
+ * The three calls chain like the contiguous ones; msa_sparse_decode_paged takes the same
+ * workspace as msa_sparse_decode (msa_workspace_bytes(shape, 1)). */
+msa_status msa_index_scores_paged(const msa_shape* shape, const int32_t* seq_lens,
+                                  const int32_t* block_table, int32_t n_phys, const void* idx_q,
+                                  const void* idx_k_pool, float* block_scores, void* stream);
+msa_status msa_block_topk_ragged(const msa_shape* shape, const int32_t* seq_lens,
+                                 const float* block_scores, int32_t* sel, void* stream);
+msa_status msa_sparse_decode_paged(const msa_shape* shape, const int32_t* seq_lens,
+                                   const int32_t* block_table, int32_t n_phys, const void* q,
+                                   const void* k_pool, const void* v_pool, const int32_t* sel,
+                                   void* out, float* lse, void* workspace, size_t ws_bytes,
+                                   void* stream);
+
 /* Scratch bytes msa_sparse_prefill (which = 0) or msa_sparse_decode (which = 1) needs for
  * this shape; 0 when none.  Returns 0 for an invalid shape. */
 size_t msa_workspace_bytes(const msa_shape* shape, int which);
@@ -152,6 +180,14 @@ const char* msa_status_string(msa_status status);
 
 /* Human-readable detail of the last failure on the calling thread ("" if none). */
 const char* msa_last_error(void);
+
+/* Test hook for the failure path.  mode 1: every tensor-core sparse-prefill launch made
+ * afterwards (from any thread) has its copy-issuing warp issue nothing, so the warps that
+ * wait for the copies give up after their one-second bound, the kernel writes zeros and
+ * -inf, and the next msa_get_device_status() reports MSA_ERR_TIMEOUT.  No copy or MMA is
+ * ever in flight in this mode, and the CUDA context stays usable.  mode 0 (default):
+ * normal operation.  Any other mode: MSA_ERR_INVALID_ARG. */
+msa_status msa_debug_set_fault(int32_t mode);
 
 /* MSA_ABI_VERSION of the loaded library. */
 int32_t msa_abi_version(void);

@@ -1,0 +1,56 @@
+"""The failure path of the tensor-core kernels, exercised without faulting the GPU.
+
+The test hook makes the prefill kernel's copy-issuing warp issue nothing, so the barrier
+the MMA warp waits on is never completed (a flag nothing sets).  Every wait in the kernel
+is bounded (one second): the kernel must give up, record MSA_ERR_TIMEOUT in the device
+status word, and leave the context usable for the next, normal call.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import oracle
+from block_sparse_gqa_02_gb300 import _lib
+from block_sparse_gqa_02_gb300.configs import CONFIGS
+from block_sparse_gqa_02_gb300.inputs import make_inputs, random_selection
+from tests.parity import check_lse, check_out
+
+import numpy as np
+
+
+def test_fault_hook_rejects_unknown_modes():
+    lib = _lib.load()
+    assert lib.msa_debug_set_fault(7) == _lib.MSA_ERR_INVALID_ARG
+    assert lib.msa_debug_set_fault(0) == _lib.MSA_OK
+
+
+@pytest.mark.gpu
+def test_bounded_wait_times_out_and_context_survives():
+    cfg = CONFIGS["p32k"].with_(seq=256, top_k=2, n_plants=0)
+    x = make_inputs(cfg, device="cuda")
+    shape = _lib.shape_from_config(cfg)
+    cur = np.array([(m * 64 + 63) // 128 for m in range(shape.n_rows)])
+    sel_np = random_selection(np.broadcast_to(cur + 1, (1, 4, shape.n_rows)), 2, 3)
+    sel = torch.from_numpy(sel_np).cuda()
+    out = torch.full_like(x["q"], 3.0)
+    lse = torch.zeros((1, cfg.n_heads_q, cfg.seq), device="cuda")
+    _lib.msa_get_device_status()                       # start from a clean status word
+    _lib.msa_debug_set_fault(1)
+    try:
+        _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+        with pytest.raises(_lib.MsaError) as ei:
+            _lib.msa_get_device_status()
+        assert ei.value.status == _lib.MSA_ERR_TIMEOUT
+    finally:
+        _lib.msa_debug_set_fault(0)
+    # the abandoned launch wrote zeros and -inf instead of leaving garbage
+    assert torch.all(out == 0)
+    assert torch.all(torch.isneginf(lse))
+    # the status word was cleared, and the context still runs the kernel correctly
+    _lib.msa_get_device_status()
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    _lib.msa_get_device_status()
+    ref_o, ref_l = oracle.sparse_attention(x["q"], x["k"], x["v"], sel_np, 128, 64)
+    check_out(out, ref_o, "bf16")
+    check_lse(lse, ref_l, "bf16")
