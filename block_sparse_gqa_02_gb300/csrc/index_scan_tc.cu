@@ -57,8 +57,14 @@ index_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __nv_bfloat
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
   const int blk0 = blockIdx.x * blocks_per_cta;
-  const int nblk = max(0, min(p.nB, blk0 + blocks_per_cta) - blk0);
+  const int L = seq_len_of(p, b);                       // this sequence's cache length
+  const int nB_b = (L + kBk - 1) / kBk;
+  const int nblk = max(0, min(nB_b, blk0 + blocks_per_cta) - blk0);
   const volatile int* abort = &s.abort;
+  // blocks of this CTA's range past the sequence's end hold no key
+  for (int blk = max(blk0, nB_b) + threadIdx.x / kNI; blk < min(p.nB, blk0 + blocks_per_cta);
+       blk += kThreads / kNI)
+    scores[((size_t)b * kNI + threadIdx.x % kNI) * p.nB + blk] = -INFINITY;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -101,9 +107,12 @@ index_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __nv_bfloat
       if (!ptx::mbar_wait(&s.empty[st], ((i / kStages) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&s.full[st], kBlockBytes);
+        // contiguous cache: (dims, key, sequence); paged pool: (dims, key in block, block)
+        const int blk = blk0 + i;
+        const int y = p.block_table ? 0 : blk * kBk;
+        const int z = p.block_table ? p.block_table[(size_t)b * p.nB + blk] : b;
         for (int kc = 0; kc < 2; ++kc)
-          ptx::tma_load_3d(s.a[st] + kc * kBk * kRowBytes, &tm_k, &s.full[st], kc * 64,
-                           (blk0 + i) * kBk, b);
+          ptx::tma_load_3d(s.a[st] + kc * kBk * kRowBytes, &tm_k, &s.full[st], kc * 64, y, z);
       }
       issued = i + 1;
       __syncwarp();
@@ -157,7 +166,7 @@ index_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __nv_bfloat
       float mx[kNI];
 #pragma unroll
       for (int h = 0; h < kNI; ++h) {
-        mx[h] = key < p.Sk ? __uint_as_float(r[h]) : -INFINITY;
+        mx[h] = key < L ? __uint_as_float(r[h]) : -INFINITY;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
       }
@@ -201,8 +210,11 @@ cudaError_t launch_index_scan_tc(const Dims& p, const void* idx_q, const void* i
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   CUtensorMap tk;
-  const uint64_t kd[3] = {(uint64_t)kDI, (uint64_t)p.Sk, (uint64_t)p.B};
-  const uint64_t ks[2] = {(uint64_t)kDI * 2, (uint64_t)p.Sk * kDI * 2};
+  // contiguous idx_k [B, L, dI] as (dI, L, B); a paged pool [P, 128, dI] as (dI, 128, P)
+  const uint64_t rows = p.block_table ? (uint64_t)kBk : (uint64_t)p.Sk;
+  const uint64_t outer = p.block_table ? (uint64_t)p.n_phys : (uint64_t)p.B;
+  const uint64_t kd[3] = {(uint64_t)kDI, rows, outer};
+  const uint64_t ks[2] = {(uint64_t)kDI * 2, rows * kDI * 2};
   const uint32_t kbx[3] = {64, (uint32_t)kBk, 1};
   e = make_tensor_map_bf16(&tk, idx_k, 3, kd, ks, kbx);
   if (e != cudaSuccess) return e;

@@ -93,6 +93,8 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
   const int G = p.G;
   const int32_t* srow = sel + (size_t)bg * p.k;
   const int i0 = split * per, i1 = min(p.k, i0 + per);
+  const int L = seq_len_of(p, b);                          // this sequence's cache length
+  const int nB_b = (L + kBk - 1) / kBk;
   const volatile int* abort = &s.abort;
 
   if (threadIdx.x == 0) {
@@ -107,7 +109,7 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 
   // the split's valid blocks, in order (entries < 0 or >= nB are skipped)
   auto block_at = [&](int i) { return srow[i]; };
-  auto valid = [&](int blk) { return blk >= 0 && blk < p.nB; };
+  auto valid = [&](int blk) { return blk >= 0 && blk < nB_b; };
 
   if (warp == kComputeWarps) {
     // ------------------------------------------------------------- TMA producer
@@ -120,11 +122,13 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (!ptx::mbar_wait(&s.empty[st], ((j / kStages) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&s.full[st], 2 * kBlockBytes);
+        // contiguous cache: (dims, key, sequence*Hkv + g); paged pool [P, Hkv, 128, d]:
+        // (dims, key in block, physical block*Hkv + g)
+        const int y = p.block_table ? 0 : blk * kBk;
+        const int z = p.block_table ? p.block_table[(size_t)b * p.nB + blk] * p.Hkv + g : bg;
         for (int kc = 0; kc < 2; ++kc) {
-          ptx::tma_load_3d(s.k[st] + kc * kBk * kRowBytes, &tm_k, &s.full[st], kc * 64,
-                           blk * kBk, bg);
-          ptx::tma_load_3d(s.v[st] + kc * kBk * kRowBytes, &tm_v, &s.full[st], kc * 64,
-                           blk * kBk, bg);
+          ptx::tma_load_3d(s.k[st] + kc * kBk * kRowBytes, &tm_k, &s.full[st], kc * 64, y, z);
+          ptx::tma_load_3d(s.v[st] + kc * kBk * kRowBytes, &tm_v, &s.full[st], kc * 64, y, z);
         }
       }
       ++j;
@@ -189,7 +193,7 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int key = blk * kBk + key0 + nt * 8 + 2 * c + (e & 1);
-          float x = key < p.Sk ? sc[nt][e] * c1 : -INFINITY;
+          float x = key < L ? sc[nt][e] * c1 : -INFINITY;
           sc[nt][e] = x;
           mx[e >> 1] = fmaxf(mx[e >> 1], x);
         }
@@ -304,8 +308,12 @@ cudaError_t launch_sparse_decode_mma(const Dims& p, const void* q, const void* k
                                      const int32_t* sel, float* ws_o, float* ws_l, int n_split,
                                      int per, cudaStream_t st, int* status) {
   CUtensorMap tk, tv;
-  const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)p.Sk, (uint64_t)p.B * p.Hkv};
-  const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)p.Sk * kD * 2};
+  // contiguous caches [B, Hkv, L, d] as (d, L, B*Hkv); paged pools [P, Hkv, 128, d] as
+  // (d, 128, P*Hkv)
+  const uint64_t rows = p.block_table ? (uint64_t)kBk : (uint64_t)p.Sk;
+  const uint64_t outer = p.block_table ? (uint64_t)p.n_phys * p.Hkv : (uint64_t)p.B * p.Hkv;
+  const uint64_t kd[3] = {(uint64_t)kD, rows, outer};
+  const uint64_t ks[2] = {(uint64_t)kD * 2, rows * kD * 2};
   const uint32_t kbx[3] = {64, (uint32_t)kBk, 1};
   cudaError_t e = make_tensor_map_bf16(&tk, k, 3, kd, ks, kbx);
   if (e == cudaSuccess) e = make_tensor_map_bf16(&tv, v, 3, kd, ks, kbx);

@@ -146,3 +146,41 @@ def random_block_scores(shape, seed: int, kind: str = "normal") -> np.ndarray:
     else:
         raise ValueError(kind)
     return x.astype(np.float32)
+
+
+def make_paged_decode_inputs(cfg: MsaConfig, seq_lens, device="cpu", seed: int | None = None,
+                             spare_blocks: int = 3):
+    """A paged decode batch: pools of physical 128-key blocks in a shuffled order.
+
+    Sequence b owns ceil(seq_lens[b] / Bk) physical blocks, listed in logical order in
+    ``block_table`` (width = the config's block count; unused entries -1).  The pools hold
+    ``spare_blocks`` extra blocks nobody owns.  Values are N(0,1) * input_scale draws from
+    one torch generator in the order q, k_pool, v_pool, idx_q, idx_k_pool; no planting.
+    """
+    seed = cfg.seed if seed is None else seed
+    rng = np.random.default_rng(seed)
+    dt = torch_dtype(cfg.dtype)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    bs, B = cfg.block_size, len(seq_lens)
+    nbs = [-(-int(L) // bs) for L in seq_lens]
+    P = sum(nbs) + spare_blocks
+    perm = rng.permutation(P)
+    table = np.full((B, cfg.n_blocks), -1, dtype=np.int32)
+    off = 0
+    for b, nb in enumerate(nbs):
+        table[b, :nb] = perm[off:off + nb]
+        off += nb
+    Hq, Hkv, d, dI = cfg.n_heads_q, cfg.n_heads_kv, cfg.head_dim, cfg.index_dim
+    s = cfg.input_scale
+    return {
+        "q": _randn((B, 1, Hq, d), gen, dev, dt, s),
+        "k_pool": _randn((P, Hkv, bs, d), gen, dev, dt, s),
+        "v_pool": _randn((P, Hkv, bs, d), gen, dev, dt, s),
+        "idx_q": _randn((B, 1, Hkv, dI), gen, dev, dt, s),
+        "idx_k_pool": _randn((P, bs, dI), gen, dev, dt, s),
+        "seq_lens": torch.tensor(np.asarray(seq_lens, dtype=np.int32), device=dev),
+        "block_table": torch.from_numpy(table).to(dev),
+        "n_phys": P,
+    }

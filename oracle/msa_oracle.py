@@ -335,3 +335,49 @@ def msa_decode(q, k_cache, v_cache, idx_q, idx_k, block_size, top_k, sm_scale=No
     sel = block_topk_decode(scores, L, block_size, top_k)
     out, lse = sparse_attention(q, k_cache, v_cache, sel, block_size, 1, sm_scale, L - 1)
     return scores, sel, out, lse
+
+
+# ---------------------------------------------------------------------------
+# Decode over a paged cache with a length per sequence
+# ---------------------------------------------------------------------------
+
+def gather_logical(pool_rows, length, block_size):
+    """One sequence's logical cache from its physical blocks: pool_rows [nb, ..., Bk, c]
+    stacked in logical order, truncated to `length` positions along the block axis."""
+    x = np.concatenate([_f64(r) for r in pool_rows], axis=-2)
+    return x[..., :length, :]
+
+
+def msa_decode_paged(q, k_pool, v_pool, idx_q, idx_k_pool, seq_lens, block_table, block_size,
+                     top_k, n_blocks, sm_scale=None, index_scale=None):
+    """Decode on a paged cache: sequence b's logical cache is the concatenation of the physical
+    blocks block_table[b, 0..nb_b-1] truncated to seq_lens[b] positions, and the step is the
+    contiguous decode on that cache (the paging is storage only).  k_pool/v_pool
+    [P, Hkv, Bk, d], idx_k_pool [P, Bk, dI].  Scores have n_blocks columns, -inf past each
+    sequence's blocks; an empty sequence gives sel -1, out 0, lse -inf."""
+    seq_lens = np.asarray(seq_lens)
+    table = np.asarray(block_table)
+    B = len(seq_lens)
+    NI = idx_q.shape[2]
+    Hq, d = q.shape[2], q.shape[3]
+    scores = np.full((B, NI, 1, n_blocks), -np.inf)
+    sel = np.full((B, NI, 1, top_k), -1, dtype=np.int32)
+    out = np.zeros((B, 1, Hq, d))
+    lse = np.full((B, Hq, 1), -np.inf)
+    for b in range(B):
+        L = int(seq_lens[b])
+        if L <= 0:
+            continue
+        nb = -(-L // block_size)
+        phys = [int(x) for x in table[b, :nb]]
+        ik = gather_logical([_rows(idx_k_pool, p) for p in phys], L, block_size)   # [L, dI]
+        kc = gather_logical([_rows(k_pool, p) for p in phys], L, block_size)       # [Hkv, L, d]
+        vc = gather_logical([_rows(v_pool, p) for p in phys], L, block_size)
+        sc_b, sel_b, o_b, l_b = msa_decode(_rows(q, slice(b, b + 1)), kc[None], vc[None],
+                                           _rows(idx_q, slice(b, b + 1)), ik[None],
+                                           block_size, top_k, sm_scale, index_scale)
+        scores[b, :, 0, :nb] = sc_b[0, :, 0, :]
+        sel[b] = sel_b[0]
+        out[b] = o_b[0]
+        lse[b] = l_b[0]
+    return scores, sel, out, lse

@@ -388,10 +388,52 @@ def pin_worked_example(o):
     assert out.shape == (1, T, 2, 1)
 
 
+def pin_paged_equals_contiguous(o):
+    """A paged cache is storage only: scattering each sequence's blocks into a pool in a
+    shuffled order and decoding through the block table equals the contiguous decode of the
+    same sequence truncated to its length."""
+    r = _rng(21)
+    bs, nb_max, Hq, Hkv, d, dI, kk = 4, 6, 4, 2, 3, 5, 2
+    lens = [1, 4, 5, 13, 24]
+    B = len(lens)
+    full_k = r.standard_normal((B, Hkv, nb_max * bs, d))
+    full_v = r.standard_normal((B, Hkv, nb_max * bs, d))
+    full_ik = r.standard_normal((B, nb_max * bs, dI))
+    q = r.standard_normal((B, 1, Hq, d))
+    iq = r.standard_normal((B, 1, Hkv, dI))
+    nbs = [-(-L // bs) for L in lens]
+    P = sum(nbs) + 2
+    perm = r.permutation(P)
+    table = np.full((B, nb_max), -1)
+    k_pool = r.standard_normal((P, Hkv, bs, d))
+    v_pool = r.standard_normal((P, Hkv, bs, d))
+    ik_pool = r.standard_normal((P, bs, dI))
+    off = 0
+    for b, nb in enumerate(nbs):
+        for j in range(nb):
+            ph = perm[off + j]
+            table[b, j] = ph
+            k_pool[ph] = full_k[b, :, j * bs:(j + 1) * bs]
+            v_pool[ph] = full_v[b, :, j * bs:(j + 1) * bs]
+            ik_pool[ph] = full_ik[b, j * bs:(j + 1) * bs]
+        off += nb
+    sc, sel, out, lse = o.msa_decode_paged(q, k_pool, v_pool, iq, ik_pool, lens, table, bs, kk,
+                                           nb_max)
+    for b, L in enumerate(lens):
+        sc1, sel1, out1, lse1 = o.msa_decode(q[b:b + 1], full_k[b:b + 1, :, :L],
+                                             full_v[b:b + 1, :, :L], iq[b:b + 1],
+                                             full_ik[b:b + 1, :L], bs, kk)
+        nb = nbs[b]
+        assert np.array_equal(sc[b, :, :, :nb], sc1[0]) and np.all(np.isneginf(sc[b, :, :, nb:]))
+        assert np.array_equal(sel[b], sel1[0])
+        assert np.allclose(out[b], out1[0], rtol=1e-13, atol=1e-13)
+        assert np.allclose(lse[b], lse1[0], rtol=1e-13, atol=1e-13)
+
+
 ALL_PINS = [
     pin_scores_block1_tile1, pin_scores_bruteforce, pin_decode_scores_bruteforce,
     pin_topk_bruteforce, pin_topk_layout, pin_full_k_bruteforce, pin_full_k_sdpa,
     pin_sparse_bruteforce, pin_rows_sum_to_one, pin_unselected_invariance,
     pin_decode_equals_prefill_row, pin_planted_selected, pin_head_diversity,
-    pin_worked_example,
+    pin_worked_example, pin_paged_equals_contiguous,
 ]

@@ -105,8 +105,9 @@ def _index_case(cfg, tiles=None):
         return to_np(scores), ref
     ref = oracle.index_block_scores_prefill(x["idx_q"], x["idx_k"], cfg.block_size, cfg.q_tile,
                                             tiles=tiles)
-    got = to_np(scores)
-    return (got if tiles is None else got[:, :, tiles]), ref
+    if tiles is None:
+        return to_np(scores), ref
+    return to_np(scores.index_select(2, torch.tensor(tiles, device=DEV))), ref
 
 
 INDEX_CASES = {
@@ -163,12 +164,12 @@ def _attn_case(cfg, sel_seed=0, tiles=None):
     torch.cuda.synchronize()
     ref_o, ref_l = oracle.sparse_attention(x["q"], x["k"], x["v"], sel_np, cfg.block_size,
                                            cfg.q_tile, None, 0, tiles)
-    got_o, got_l = to_np(out), to_np(lse)
-    if tiles is not None:
-        rows = np.concatenate([np.arange(m * cfg.q_tile, min(cfg.seq, (m + 1) * cfg.q_tile))
-                               for m in tiles])
-        got_o, got_l = got_o[:, rows], got_l[:, :, rows]
-    return got_o, got_l, ref_o, ref_l
+    if tiles is None:
+        return to_np(out), to_np(lse), ref_o, ref_l
+    rows = np.concatenate([np.arange(m * cfg.q_tile, min(cfg.seq, (m + 1) * cfg.q_tile))
+                           for m in tiles])
+    r_idx = torch.from_numpy(rows).to(DEV)
+    return to_np(out.index_select(1, r_idx)), to_np(lse.index_select(2, r_idx)), ref_o, ref_l
 
 
 ATTN_CASES = {
@@ -250,23 +251,31 @@ def _pipeline(cfg, tiles=None):
         sc, sel, o, l = oracle.msa_prefill(x["q"], x["k"], x["v"], x["idx_q"], x["idx_k"],
                                            cfg.block_size, cfg.q_tile, cfg.top_k, tiles=tiles)
         rows = list(range(shape.n_rows)) if tiles is None else tiles
-    g_sc, g_sel = to_np(bufs["scores"])[:, :, rows], to_np(bufs["sel"])[:, :, rows]
+    # only the sampled rows leave the GPU
+    qt = cfg.q_tile
+    r_idx = torch.tensor(rows, device=DEV)
+    tok = np.concatenate([np.arange(m * qt, min(cfg.seq_q, (m + 1) * qt)) for m in rows])
+    t_idx = torch.from_numpy(tok).to(DEV)
+    g_sc = to_np(bufs["scores"].index_select(2, r_idx))
+    g_sel = to_np(bufs["sel"].index_select(2, r_idx))
+    g_o = to_np(bufs["out"].index_select(1, t_idx))
+    g_l = to_np(bufs["lse"].index_select(2, t_idx))
     check_scores(g_sc, sc, cfg.name)
     cb = np.broadcast_to(cur_blocks(shape)[rows], g_sel.shape[:-1])
     agree = check_selection_valid(g_sel, sel, sc, cb, cfg.name)
     # attention parity on the rows whose selection matches the oracle's
-    g_o, g_l = to_np(bufs["out"]), to_np(bufs["lse"])
-    qt = cfg.q_tile
+    r0 = 0
     for i, m in enumerate(rows):
-        t = np.arange(m * qt, min(cfg.seq_q, (m + 1) * qt))
-        r = np.arange(i * qt, i * qt + len(t))
+        n = min(cfg.seq_q, (m + 1) * qt) - m * qt
+        r = np.arange(r0, r0 + n)
+        r0 += n
         for b in range(cfg.batch):
             for g in range(cfg.n_heads_kv):
                 if not np.array_equal(g_sel[b, g, i], sel[b, g, i]):
                     continue
                 hs = np.arange(g * cfg.group, (g + 1) * cfg.group)
-                check_out(g_o[b][np.ix_(t, hs)], o[b][np.ix_(r, hs)], cfg.dtype, cfg.name)
-                check_lse(g_l[b][np.ix_(hs, t)], l[b][np.ix_(hs, r)], cfg.dtype, cfg.name)
+                check_out(g_o[b][np.ix_(r, hs)], o[b][np.ix_(r, hs)], cfg.dtype, cfg.name)
+                check_lse(g_l[b][np.ix_(hs, r)], l[b][np.ix_(hs, r)], cfg.dtype, cfg.name)
     return agree
 
 
@@ -298,6 +307,17 @@ def test_pipeline_bf16_small():
 def test_pipeline_p32k_sampled():
     cfg = CONFIGS["p32k"]
     assert _pipeline(cfg, tiles=sample_tiles(cfg.n_tiles, seed=4)) >= 0.9
+
+
+def test_pipeline_p128k_sampled():
+    cfg = CONFIGS["p128k"]
+    assert _pipeline(cfg, tiles=sample_tiles(cfg.n_tiles, seed=5)) >= 0.9
+
+
+def test_pipeline_p1m_sampled():
+    """The 1M-context prefill, run in full on the GPU, checked on sampled tiles."""
+    cfg = CONFIGS["p1m"]
+    assert _pipeline(cfg, tiles=sample_tiles(cfg.n_tiles, n_random=1, seed=6)) >= 0.9
 
 
 def test_pipeline_d1m():
