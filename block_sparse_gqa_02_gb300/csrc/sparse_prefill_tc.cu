@@ -327,13 +327,14 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::tmem_ld_wait();
       // keys j > t are masked; only a block reaching past this row's token needs it
       const int lim = t - blk * kBk;                         // visible columns: c <= lim
-      float mx = -INFINITY;
+      // four independent max chains (one per 32-column chunk) keep the dependency short
+      float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (lim >= kBk - 1) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            mx = max3(mx, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            mc[c] = max3(mc[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
       } else {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -341,9 +342,10 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int e = 0; e < 32; ++e) {
             const float x = c * 32 + e <= lim ? __uint_as_float(sv[c][e]) : -INFINITY;
             sv[c][e] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+            mc[c] = fmaxf(mc[c], x);
           }
       }
+      const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
       const float mb = mx * c1;                              // block max, log2 units
       float alpha = 1.f;
       bool rescale = false;
@@ -358,23 +360,23 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const float m_eff = m_used == -INFINITY ? 0.f : m_used;
       // p = 2^(s * c1 - m): pairs of columns through packed fp32 FMA / ADD
       const uint64_t c1x2 = f32x2(c1, c1), negm = f32x2(-m_eff, -m_eff);
-      uint64_t acc0 = f32x2(0.f, 0.f), acc1 = acc0;
+      uint64_t acc[4];                                       // one sum chain per chunk
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
+        acc[c] = f32x2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const uint64_t y = fma_f32x2(f32x2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])),
                                        c1x2, negm);
           const float p0 = ex2(lo_f32(y)), p1 = ex2(hi_f32(y));
-          const uint64_t pp = f32x2(p0, p1);
-          if ((e >> 1) & 1) acc1 = add_f32x2(acc1, pp); else acc0 = add_f32x2(acc0, pp);
+          acc[c] = add_f32x2(acc[c], f32x2(p0, p1));
           pk[e >> 1] = pack_bf16x2(p0, p1);
         }
         ptx::tmem_st_x16(s_addr + c * 16, pk);
       }
-      const uint64_t acc = add_f32x2(acc0, acc1);
-      l += lo_f32(acc) + hi_f32(acc);
+      const uint64_t accs = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
+      l += lo_f32(accs) + hi_f32(accs);
       if (rescale) {
         // P.V of the previous block is complete (it precedes this block's Q.K^T); O is
         // rescaled before this block's P is released to the MMA warp
