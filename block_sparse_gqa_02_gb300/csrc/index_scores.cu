@@ -185,7 +185,7 @@ cudaError_t launch_index_scores(const Dims& p, const void* idx_q, const void* id
                                 float* scores, cudaStream_t st, int* dev_status) {
   if (p.dtype == 1) {
     if (index_tc_supported(p))
-      return launch_index_scores_tc(p, idx_q, idx_k, scores, st, dev_status);
+      return launch_index_scores_tc(p, idx_q, idx_k, scores, nullptr, st, dev_status);
     if (index_scan_tc_supported(p))
       return launch_index_scan_tc(p, idx_q, idx_k, scores, st, dev_status);
     return dispatch_dim<__nv_bfloat16>(p, idx_q, idx_k, scores, st);

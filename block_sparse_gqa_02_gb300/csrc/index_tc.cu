@@ -37,6 +37,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = (kEpiWarps + 2) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kBk);
+constexpr int kMaxWant = 255;      // fused top-k: up to 255 blocks besides the current one
 
 struct __align__(1024) Smem {
   uint8_t a[kABytes];
@@ -45,6 +46,9 @@ struct __align__(1024) Smem {
   uint64_t a_full, acc_full[2], acc_empty[2];
   uint64_t pair_bar[kEpiWarps / 2][2];
   float part[2][kEpiWarps];
+  // fused top-k: per head, the best blocks seen so far (unordered) and how many
+  float tk_s[kNI][kMaxWant];
+  int tk_i[kNI][kMaxWant];
   uint32_t tmem_base;
   int abort;
 };
@@ -57,7 +61,7 @@ __device__ __forceinline__ void raise_abort(Smem& s, int* status, int code) {
 __global__ void __launch_bounds__(kThreads, 1)
 index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k, float* __restrict__ scores,
-                       Dims p, int* status) {
+                       int32_t* __restrict__ sel, Dims p, int* status) {
   extern __shared__ uint8_t smem_raw[];
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
@@ -90,11 +94,12 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     ptx::tmem_relinquish();
   }
   // scores layout [B, NI, nR, nB]; blocks after the current one see no key
-  float* srow = scores + ((size_t)b * kNI * p.nR + m) * p.nB;
+  float* srow = scores ? scores + ((size_t)b * kNI * p.nR + m) * p.nB : nullptr;
   const size_t head_stride = (size_t)p.nR * p.nB;
   const int n_after = p.nB - nblk;
-  for (int i = threadIdx.x; i < kNI * n_after; i += kThreads)
-    srow[(size_t)(i / n_after) * head_stride + nblk + i % n_after] = -INFINITY;
+  if (scores)
+    for (int i = threadIdx.x; i < kNI * n_after; i += kThreads)
+      srow[(size_t)(i / n_after) * head_stride + nblk + i % n_after] = -INFINITY;
   ptx::tc_fence_before_sync();
   __syncthreads();
   ptx::tc_fence_after_sync();
@@ -184,6 +189,11 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const bool valid = t < p.Sq;
     const int pair = warp >> 1;
     bool ok = true;
+    // fused top-k state of this head (used by the even warp of the pair, all lanes)
+    const int want = sel ? min(p.k - 1, cb) : 0;   // blocks kept besides the current one
+    int n_kept = 0, worst_pos = 0;
+    float worst_s = INFINITY;
+    bool search = false;
     for (int i = 0; i < nblk; ++i) {
       const int buf = i & 1;
       const uint32_t bph = (i >> 1) & 1;
@@ -221,10 +231,62 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         ptx::mbar_arrive(&s.pair_bar[pair][i & 1]);
       }
       if (!ptx::mbar_wait(&s.pair_bar[pair][i & 1], (i >> 1) & 1, abort)) { ok = false; break; }
-      if ((warp & 1) == 0 && lane == 0) {
+      if ((warp & 1) == 0) {
         const float v = fmaxf(s.part[i & 1][warp], s.part[i & 1][warp + 1]);
-        srow[(size_t)head * head_stride + i] = v == -INFINITY ? -INFINITY : v * p.index_scale;
+        const float score = v == -INFINITY ? -INFINITY : v * p.index_scale;
+        if (srow && lane == 0) srow[(size_t)head * head_stride + i] = score;
+        if (i < cb && want > 0) {
+          // blocks arrive in index order, so a newcomer displaces the worst kept block only
+          // when its score is strictly higher (on a tie the lower index stays)
+          if (n_kept < want) {
+            if (lane == 0) {
+              s.tk_s[head][n_kept] = score;
+              s.tk_i[head][n_kept] = i;
+            }
+            ++n_kept;
+            search = n_kept == want;
+          } else if (score > worst_s) {
+            if (lane == 0) {
+              s.tk_s[head][worst_pos] = score;
+              s.tk_i[head][worst_pos] = i;
+            }
+            search = true;
+          }
+          if (search) {
+            search = false;
+            __syncwarp();
+            // the worst kept block: lowest score, and of equal scores the highest index
+            float ws = INFINITY;
+            int wi = -1, wp = 0;
+            for (int e = lane; e < want; e += 32) {
+              const float cs = s.tk_s[head][e];
+              const int ci = s.tk_i[head][e];
+              if (cs < ws || (cs == ws && ci > wi)) { ws = cs; wi = ci; wp = e; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              const float os = __shfl_xor_sync(0xffffffffu, ws, o);
+              const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+              const int op = __shfl_xor_sync(0xffffffffu, wp, o);
+              if (os < ws || (os == ws && oi > wi)) { ws = os; wi = oi; wp = op; }
+            }
+            worst_s = ws;
+            worst_pos = wp;
+          }
+          __syncwarp();
+        }
       }
+    }
+    if (ok && sel && (warp & 1) == 0) {
+      // kept blocks in ascending index order, then the current block, then -1 padding
+      int32_t* out = sel + (((size_t)b * kNI + head) * p.nR + m) * p.k;
+      for (int e = lane; e < n_kept; e += 32) {
+        const int ci = s.tk_i[head][e];
+        int rank = 0;
+        for (int f = 0; f < n_kept; ++f) rank += s.tk_i[head][f] < ci;
+        out[rank] = ci;
+      }
+      for (int e = n_kept + lane; e < p.k; e += 32) out[e] = e == n_kept ? cb : -1;
     }
     if (!ok && lane == 0) raise_abort(s, status, 0x103);
   }
@@ -239,13 +301,15 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 }  // namespace
 
+bool index_topk_fused_supported(const Dims& p) { return index_tc_supported(p) && p.k <= kMaxWant + 1; }
+
 bool index_tc_supported(const Dims& p) {
   return p.dtype == 1 && !p.decode && p.dI == kDI && p.Bk == kBk && p.Qt == kQt &&
          p.Hkv == kNI;
 }
 
 cudaError_t launch_index_scores_tc(const Dims& p, const void* idx_q, const void* idx_k,
-                                   float* scores, cudaStream_t st, int* status) {
+                                   float* scores, int32_t* sel, cudaStream_t st, int* status) {
   CUtensorMap tq, tk;
   // idx_q [B, T, NI, dI] as (dI, NI, T, B); one box = 64 dims x 1 head x 64 tokens
   const uint64_t qd[4] = {(uint64_t)kDI, (uint64_t)kNI, (uint64_t)p.Sq, (uint64_t)p.B};
@@ -265,7 +329,7 @@ cudaError_t launch_index_scores_tc(const Dims& p, const void* idx_q, const void*
                            (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.nR, p.B);
-  index_scores_tc_kernel<<<grid, kThreads, smem, st>>>(tq, tk, scores, p, status);
+  index_scores_tc_kernel<<<grid, kThreads, smem, st>>>(tq, tk, scores, sel, p, status);
   return cudaGetLastError();
 }
 

@@ -4,6 +4,8 @@
 
 namespace msa {
 bool index_tc_supported(const Dims& p);
+bool index_topk_fused_supported(const Dims& p);
+// scores may be null when sel is given (fused top-k); sel null = scores only.
 cudaError_t launch_index_scores_tc(const Dims& p, const void* idx_q, const void* idx_k,
-                                   float* scores, cudaStream_t st, int* status);
+                                   float* scores, int32_t* sel, cudaStream_t st, int* status);
 }  // namespace msa

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include "common.cuh"
+#include "index_tc.cuh"
 #include "msa.h"
 
 namespace msa {
@@ -144,6 +145,24 @@ msa_status msa_index_scores(const msa_shape* shape, const void* idx_q, const voi
   cudaError_t e = launch_index_scores(d, idx_q, idx_k, block_scores, (cudaStream_t)stream,
                                       status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_scores launch");
+}
+
+msa_status msa_index_topk_fused(const msa_shape* shape, const void* idx_q, const void* idx_k,
+                                float* block_scores, int32_t* sel, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  MSA_TRY(check_ptr(idx_q, "idx_q"));
+  MSA_TRY(check_ptr(idx_k, "idx_k"));
+  MSA_TRY(check_ptr(block_scores, "block_scores", true));
+  MSA_TRY(check_ptr(sel, "sel"));
+  if (!index_topk_fused_supported(d))
+    return fail(MSA_ERR_UNSUPPORTED,
+                "fused index + top-k runs bf16 prefill with index_dim 128, block 128, q_tile "
+                "64, 4 KV heads and top_k <= 256");
+  cudaError_t e = launch_index_scores_tc(d, idx_q, idx_k, block_scores, sel,
+                                         (cudaStream_t)stream, status_ptr());
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_topk_fused launch");
 }
 
 msa_status msa_block_topk(const msa_shape* shape, const float* block_scores, int32_t* sel,

@@ -100,6 +100,16 @@ msa_status msa_index_scores(const msa_shape* shape, const void* idx_q, const voi
 msa_status msa_block_topk(const msa_shape* shape, const float* block_scores, int32_t* sel,
                           void* stream);
 
+/* msa_index_scores followed by msa_block_topk in one launch, without the block-score round
+ * trip through HBM: the index kernel keeps each KV head's running best top_k-1 blocks as
+ * the scores of successive blocks come out of the tensor cores, and writes sel directly
+ * (same selection rule, bit-identical to the two calls).  block_scores may be NULL; when
+ * given, it is filled as by msa_index_scores.  bf16 prefill with index_dim 128,
+ * block_size 128, q_tile 64, 4 KV heads and top_k <= 256; other shapes get
+ * MSA_ERR_UNSUPPORTED. */
+msa_status msa_index_topk_fused(const msa_shape* shape, const void* idx_q, const void* idx_k,
+                                float* block_scores, int32_t* sel, void* stream);
+
 /* Main branch, prefill (seq_q == seq_k): for query t and head h (KV head g), attend over the
  * keys j <= t of the blocks listed in sel[b, g, t / q_tile, :] (entries -1 are skipped;
  * entries must be distinct).  Writes out (dtype) and, if lse != NULL, lse.  A row whose key
