@@ -64,6 +64,31 @@ def decode_bytes(cfg):
     return scan, kv + rest, dense
 
 
+# DRAM traffic per launch from ncu captures (profiles/), valid only for the kernel source
+# that was profiled: a changed kernel reports null until it is captured again.
+MEASURED_TRAFFIC = {
+    "sparse_prefill_tc.cu": {
+        "sha256_16": "6983e3bc97910a68",
+        "workload": "p128k",
+        "bytes_per_launch": 4.53e9,
+        "how": "dram__bytes_read.sum + dram__bytes_write.sum of one p32k launch "
+               "(336.2 + 229.5 MB), scaled by the (token, query head) rows to 128K (x8)",
+    },
+}
+
+
+def measured_traffic(kernel_file: str, workload: str):
+    import hashlib
+    rec = MEASURED_TRAFFIC.get(kernel_file)
+    if rec is None or rec["workload"] != workload:
+        return None
+    path = os.path.join(ROOT, "block_sparse_gqa_02_gb300", "csrc", kernel_file)
+    with open(path, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["sha256_16"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -352,7 +377,9 @@ def run_ours(args, rank, world, device):
                    "timing": "CUDA events on the launching stream around the library calls"},
         "roofline": {"bound": "tensor", "kernel": "sparse prefill attention",
                      "achieved": attn_tf, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": attn_tf / tc_peak, "traffic": None,
+                     "frac": attn_tf / tc_peak,
+                     "traffic": measured_traffic("sparse_prefill_tc.cu", pcfg.name),
+                     "traffic_note": MEASURED_TRAFFIC["sparse_prefill_tc.cu"]["how"],
                      "peak_source": f"{peak_src} bf16 sustained",
                      "algorithmic_flops_per_launch": f_sparse},
         "kernels_ms": {"index_scores": k_idx, "block_topk": k_topk, "sparse_prefill": k_attn},
@@ -432,6 +459,78 @@ def run_reference(args):
     }
 
 
+# ------------------------------------------------------------------ ablations
+
+def run_ablation(args):
+    """What MSA's two changes to DSA buy, measured on synthetic inputs:
+    * per-KV-head vs shared (aggregated) selection: recall of each head's planted blocks on
+      the 32K planted workload (MSA keeps heads diverse; sharing loses their own plants);
+    * block-level vs token-level top-k: time and score-tensor size of the selection step
+      at 16K tokens for the same number of attended keys (k blocks of 128 vs 128k tokens).
+    """
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    cfg = CONFIGS["p32k"]
+    x = make_inputs(cfg, device=dev)
+    shape = _lib.shape_from_config(cfg)
+    dims = (1, 4, shape.n_rows)
+    sc = torch.empty(dims + (shape.n_blocks,), device=dev)
+    own = torch.empty(dims + (cfg.top_k,), dtype=torch.int32, device=dev)
+    shared = torch.empty_like(own)
+    _lib.msa_index_scores(shape, x["idx_q"], x["idx_k"], sc)
+    _lib.msa_block_topk(shape, sc, own)
+    _lib.msa_block_topk_shared(shape, sc, shared)
+    torch.cuda.synchronize()
+    own_np, sh_np = own.cpu().numpy(), shared.cpu().numpy()
+
+    def recall(sel):
+        hit = tot = 0
+        for g in range(4):
+            for m in range(shape.n_rows):
+                cur = (m * 64 + 63) // 128
+                for pl in x["plants"][0, g]:
+                    if pl < cur:
+                        tot += 1
+                        hit += int(pl in sel[0, g, m])
+        return hit / max(tot, 1)
+    distinct = float(np.mean([len({tuple(own_np[0, g, m]) for g in range(4)}) > 1
+                              for m in range(shape.n_rows)]))
+
+    def time_topk(T, bs, qt, k, reps=10):
+        sh = _lib.make_shape(1, T, T, 16, 4, 128, 128, bs, k, qt, "bf16")
+        scores = torch.randn((1, 4, sh.n_rows, sh.n_blocks), device=dev)
+        sel = torch.empty((1, 4, sh.n_rows, k), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            _lib.msa_block_topk(sh, scores, sel)
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record()
+            _lib.msa_block_topk(sh, scores, sel)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        out = {"rows": 4 * sh.n_rows, "candidates_per_row_max": sh.n_blocks, "k": k,
+               "ms": float(np.median(ts)), "score_tensor_bytes": scores.numel() * 4}
+        del scores, sel
+        torch.cuda.empty_cache()
+        return out
+    T = 16384
+    blk = time_topk(T, 128, 64, 16)
+    tok = time_topk(T, 1, 1, 16 * 128)
+    return {"ablation": "per-KV-head block selection vs shared selection and token-level top-k",
+            "data": "synthetic",
+            "head_diversity": {"workload": f"{cfg.name}: {cfg.description}",
+                               "per_head_plant_recall": recall(own_np),
+                               "shared_plant_recall": recall(sh_np),
+                               "rows_where_heads_differ": distinct},
+            "topk_cost": {"seq": T, "block_level": blk, "token_level": tok,
+                          "time_ratio": tok["ms"] / blk["ms"],
+                          "score_bytes_ratio": tok["score_tensor_bytes"] /
+                          blk["score_tensor_bytes"]}}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -449,6 +548,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ablation", action="store_true",
+                    help="print the selection ablations (shared / token-level) instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -456,6 +557,10 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.ablation:
+        if rank == 0:
+            print(json.dumps(run_ablation(args)), flush=True)
+        return 0
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)

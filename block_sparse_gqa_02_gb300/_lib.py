@@ -42,6 +42,7 @@ SIGNATURES = {
     "msa_index_scores": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp]),
     "msa_block_topk": (_i32, [_SHAPE_P, _vp, _vp, _vp]),
     "msa_index_topk_fused": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp]),
+    "msa_block_topk_shared": (_i32, [_SHAPE_P, _vp, _vp, _vp]),
     "msa_sparse_prefill": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode_static": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -144,6 +145,12 @@ def msa_index_scores(shape: MsaShape, idx_q, idx_k, block_scores, stream=None):
 def msa_block_topk(shape: MsaShape, block_scores, sel, stream=None):
     _check(load().msa_block_topk(ctypes.byref(shape), _ptr(block_scores), _ptr(sel),
                                  _stream(stream)), "msa_block_topk")
+
+
+def msa_block_topk_shared(shape: MsaShape, block_scores, sel, stream=None):
+    """Ablation: one selection per row from the KV heads' summed scores, shared by all heads."""
+    _check(load().msa_block_topk_shared(ctypes.byref(shape), _ptr(block_scores), _ptr(sel),
+                                        _stream(stream)), "msa_block_topk_shared")
 
 
 def msa_index_topk_fused(shape: MsaShape, idx_q, idx_k, sel, block_scores=None, stream=None):

@@ -52,9 +52,13 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_sums, int& to
   return before;
 }
 
+// shared != 0: the row is (b, m) and its candidates are the fp32 sums over the KV heads of
+// their block scores (added in head order 0, 1, ...); the one selection is written to every
+// head's row (the aggregated selection the pages contrast MSA with).
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __restrict__ scores,
-                                                              int32_t* __restrict__ sel, Dims p) {
+                                                              int32_t* __restrict__ sel, Dims p,
+                                                              int shared) {
   constexpr int kWarps = kThreads / 32;
   extern __shared__ uint32_t keys[];                        // [cb]
   __shared__ uint32_t hist[256];
@@ -62,29 +66,45 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
   __shared__ uint32_t s_digit;
   __shared__ int s_remaining;
 
-  const int row = blockIdx.x;                               // (b * Hkv + g) * nR + m
+  // row = (b * Hkv + g) * nR + m, or b * nR + m for the shared selection
+  const int row = blockIdx.x;
   const int m = row % p.nR;
+  const int b = shared ? row / p.nR : row / (p.Hkv * p.nR);
   // ragged decode: the query of sequence b sits at its own cache length - 1
-  const int last = p.seq_lens ? seq_len_of(p, row / (p.Hkv * p.nR)) - 1 : row_last_pos(p, m);
+  const int last = p.seq_lens ? seq_len_of(p, b) - 1 : row_last_pos(p, m);
   const float* srow = scores + (size_t)row * p.nB;
   int32_t* out = sel + (size_t)row * p.k;
+  const size_t head_stride = (size_t)p.nR * p.nB;           // between heads, same (b, m)
+  if (shared) {
+    srow = scores + ((size_t)b * p.Hkv * p.nR + m) * p.nB;
+    out = sel + ((size_t)b * p.Hkv * p.nR + m) * p.k;
+  }
+  const int n_out = shared ? p.Hkv : 1;
+  const size_t out_stride = (size_t)p.nR * p.k;
   if (last < 0) {                                           // empty sequence: nothing visible
-    for (int i = threadIdx.x; i < p.k; i += kThreads) out[i] = -1;
+    for (int h = 0; h < n_out; ++h)
+      for (int i = threadIdx.x; i < p.k; i += kThreads) out[h * out_stride + i] = -1;
     return;
   }
   const int cb = last / p.Bk;
 
   if (cb + 1 <= p.k) {                                      // every candidate fits
-    for (int i = threadIdx.x; i < p.k; i += kThreads) out[i] = i <= cb ? i : -1;
+    for (int h = 0; h < n_out; ++h)
+      for (int i = threadIdx.x; i < p.k; i += kThreads) out[h * out_stride + i] = i <= cb ? i : -1;
     return;
   }
   const int want = p.k - 1;                                 // picked from blocks 0..cb-1
   if (want == 0) {
-    if (threadIdx.x == 0) out[0] = cb;
+    if (threadIdx.x < n_out) out[threadIdx.x * out_stride] = cb;
     return;
   }
   const int n = cb;
-  for (int i = threadIdx.x; i < n; i += kThreads) keys[i] = order_key(srow[i]);
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    float x = srow[i];
+    if (shared)
+      for (int h = 1; h < p.Hkv; ++h) x = __fadd_rn(x, srow[h * head_stride + i]);
+    keys[i] = order_key(x);
+  }
 
   // radix select of the want-th largest key, 8 bits at a time from the top
   uint32_t prefix = 0, mask = 0;
@@ -157,33 +177,37 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
     for (int i = lo; i < hi; ++i) {
       const uint32_t key = keys[i];
       const bool take = key > tau || (key == tau && rank++ < take_eq);
-      if (take) out[pos++] = i;
+      if (take) {
+        for (int h = 0; h < n_out; ++h) out[h * out_stride + pos] = i;
+        ++pos;
+      }
     }
   }
-  if (threadIdx.x == 0) out[want] = cb;                     // cb > every earlier block
+  if (threadIdx.x < n_out) out[threadIdx.x * out_stride + want] = cb;   // cb > every earlier
 }
 
 }  // namespace
 
 template <int kThreads>
-static cudaError_t launch_rows(const Dims& p, const float* scores, int32_t* sel, cudaStream_t st) {
-  const int rows = p.B * p.Hkv * p.nR;
+static cudaError_t launch_rows(const Dims& p, const float* scores, int32_t* sel, cudaStream_t st,
+                               int shared) {
+  const int rows = shared ? p.B * p.nR : p.B * p.Hkv * p.nR;
   const size_t smem = (size_t)p.nB * sizeof(uint32_t);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(block_topk_kernel<kThreads>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  block_topk_kernel<kThreads><<<rows, kThreads, smem, st>>>(scores, sel, p);
+  block_topk_kernel<kThreads><<<rows, kThreads, smem, st>>>(scores, sel, p, shared);
   return cudaGetLastError();
 }
 
 cudaError_t launch_block_topk(const Dims& p, const float* scores, int32_t* sel,
-                              cudaStream_t st) {
+                              cudaStream_t st, int shared) {
   if (p.B * p.Hkv * p.nR == 0) return cudaSuccess;
   // long rows (decode at 1M context: 8192 candidates) get more threads per row
-  if (p.nB > 2048) return launch_rows<1024>(p, scores, sel, st);
-  return launch_rows<256>(p, scores, sel, st);
+  if (p.nB > 2048) return launch_rows<1024>(p, scores, sel, st, shared);
+  return launch_rows<256>(p, scores, sel, st, shared);
 }
 
 }  // namespace msa

@@ -73,8 +73,10 @@ template <> struct Vec16<__nv_bfloat16> {
 // Each returns the launch error (cudaSuccess when the kernel was queued).
 cudaError_t launch_index_scores(const Dims& p, const void* idx_q, const void* idx_k,
                                 float* scores, cudaStream_t st, int* dev_status);
+// shared = 1: one selection per (sequence, row) from the heads' summed scores, written to
+// every head (the aggregated selection used as an ablation)
 cudaError_t launch_block_topk(const Dims& p, const float* scores, int32_t* sel,
-                              cudaStream_t st);
+                              cudaStream_t st, int shared = 0);
 cudaError_t launch_sparse_prefill(const Dims& p, const void* q, const void* k,
                                   const void* v, const int32_t* sel, void* out, float* lse,
                                   cudaStream_t st, int* dev_status);

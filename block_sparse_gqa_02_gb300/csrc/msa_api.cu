@@ -147,6 +147,17 @@ msa_status msa_index_scores(const msa_shape* shape, const void* idx_q, const voi
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_scores launch");
 }
 
+msa_status msa_block_topk_shared(const msa_shape* shape, const float* block_scores,
+                                 int32_t* sel, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  MSA_TRY(check_ptr(block_scores, "block_scores"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  cudaError_t e = launch_block_topk(d, block_scores, sel, (cudaStream_t)stream, 1);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_block_topk_shared launch");
+}
+
 msa_status msa_index_topk_fused(const msa_shape* shape, const void* idx_q, const void* idx_k,
                                 float* block_scores, int32_t* sel, void* stream) {
   g_last_error[0] = 0;

@@ -100,6 +100,15 @@ msa_status msa_index_scores(const msa_shape* shape, const void* idx_q, const voi
 msa_status msa_block_topk(const msa_shape* shape, const float* block_scores, int32_t* sel,
                           void* stream);
 
+/* Ablation, not MSA: the aggregated selection the pages contrast MSA with (DSA-style, one
+ * token set shared by every KV head).  For each (sequence, row) the candidates' scores are
+ * the fp32 sums of the KV heads' block scores, added in head order 0, 1, ...; one selection
+ * by the same rule as msa_block_topk is written to every head's row of sel.  Used to
+ * measure the head-diversity loss of sharing ("Sparse Attention Cannot Be Directly Ported
+ * Across Architectures", paragraph on applying DSA to GQA). */
+msa_status msa_block_topk_shared(const msa_shape* shape, const float* block_scores,
+                                 int32_t* sel, void* stream);
+
 /* msa_index_scores followed by msa_block_topk in one launch, without the block-score round
  * trip through HBM: the index kernel keeps each KV head's running best top_k-1 blocks as
  * the scores of successive blocks come out of the tensor cores, and writes sel directly

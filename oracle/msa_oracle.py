@@ -381,3 +381,24 @@ def msa_decode_paged(q, k_pool, v_pool, idx_q, idx_k_pool, seq_lens, block_table
         out[b] = o_b[0]
         lse[b] = l_b[0]
     return scores, sel, out, lse
+
+
+# ---------------------------------------------------------------------------
+# Ablation: one selection shared by all KV heads (what MSA does not do)
+# ---------------------------------------------------------------------------
+
+def block_topk_shared_prefill(scores, seq_len, q_tile, block_size, top_k):
+    """The aggregated selection the pages contrast MSA with ("Sparse Attention Cannot Be
+    Directly Ported Across Architectures", paragraph on applying DSA to GQA: aggregating the
+    index output into one selection makes every KV head attend to the same set).  The heads'
+    block scores are summed -- in float32, in head order, since the sum decides an integer
+    selection and is taken in the precision the kernel uses -- and one selection by the usual
+    rule is given to every head."""
+    sc = np.asarray(scores, dtype=np.float32)
+    B, NI, nT, nB = sc.shape
+    agg = sc[:, 0].copy()
+    for g in range(1, NI):
+        agg = (agg + sc[:, g]).astype(np.float32)
+    one = block_topk_prefill(agg[:, None].astype(np.float64), seq_len, q_tile, block_size,
+                             top_k)
+    return np.repeat(one, NI, axis=1)

@@ -67,6 +67,30 @@ def test_topk_bit_exact(case):
         f"{got[tuple(bad[0])]} vs {ref[tuple(bad[0])]}"
 
 
+@pytest.mark.parametrize("kind", ["normal", "ties", "mixed"])
+def test_topk_shared_bit_exact(kind):
+    """The aggregated (shared across heads) selection used for the ablation."""
+    T, bs, qt, k = 20000, 128, 64, 16
+    shape = _lib.make_shape(2, T, T, 32, 4, 128, 128, bs, k, qt, "bf16")
+    sc = random_block_scores((2, 4, shape.n_rows, shape.n_blocks), seed=11, kind=kind)
+    sel = torch.full((2, 4, shape.n_rows, k), -7, dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk_shared(shape, torch.from_numpy(sc).to(DEV), sel)
+    ref = oracle.block_topk_shared_prefill(sc, T, qt, bs, k)
+    assert np.array_equal(sel.cpu().numpy(), ref)
+
+
+def test_topk_token_level_bit_exact():
+    """Token-level selection (block size 1, one query per row), the other ablation."""
+    T, k = 3000, 200
+    shape = _lib.make_shape(1, T, T, 16, 4, 64, 64, 1, k, 1, "bf16")
+    sc = random_block_scores((1, 4, T, T), seed=12, kind="mixed")
+    sel = torch.empty((1, 4, T, k), dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk(shape, torch.from_numpy(sc).to(DEV), sel)
+    rows = sample_tiles(T, n_random=40, seed=4)
+    ref = oracle.block_topk_prefill(sc[:, :, rows], T, 1, 1, k, tiles=rows)
+    assert np.array_equal(sel.cpu().numpy()[:, :, rows], ref)
+
+
 @pytest.mark.parametrize("kind", ["normal", "ties"])
 def test_topk_decode_1m_bit_exact(kind):
     B, L, bs, k = 8, 1 << 20, 128, 64
