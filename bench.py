@@ -224,34 +224,68 @@ class Step:
 
 
 def e2e_prefill(cfg, step, stream, n_steps):
-    """The same metric through the public API with host buffers: pinned H2D copies of the
-    step's inputs, the three library calls, D2H of out and lse, per step."""
+    """The same metric through the public API with host buffers.  Every step copies its own
+    inputs (q, k, v, idx_q, idx_k) from pinned host memory to the device, runs the three
+    library calls, and copies out and lse back to pinned host memory.  Steps are pipelined
+    the way a serving loop runs them: three streams (copy in, compute, copy out) and two
+    sets of device buffers, so step i+1's inputs and step i-1's outputs move while step i
+    computes.  The serial figure (copy in, compute, copy out, then the next step) is
+    reported alongside."""
     names = ["q", "k", "v", "idx_q", "idx_k"]
+    dev0 = step.x["q"].device
     host = {n: step.x[n].cpu().pin_memory() for n in names}
-    out_h = torch.empty(step.bufs["out"].shape, dtype=step.bufs["out"].dtype).pin_memory()
-    lse_h = torch.empty(step.bufs["lse"].shape, dtype=torch.float32).pin_memory()
+    out_h = [torch.empty(step.bufs["out"].shape, dtype=step.bufs["out"].dtype).pin_memory()
+             for _ in range(2)]
+    lse_h = [torch.empty(step.bufs["lse"].shape, dtype=torch.float32).pin_memory()
+             for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
-    dev = {n: torch.empty_like(step.x[n]) for n in names}
-    times = []
-    with torch.cuda.stream(stream):
-        for i in range(n_steps + 1):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for n in names:
-                dev[n].copy_(host[n], non_blocking=True)
-            api.run_prefill(step.shape, dev["q"], dev["k"], dev["v"], dev["idx_q"],
-                            dev["idx_k"], step.bufs, stream)
-            out_h.copy_(step.bufs["out"], non_blocking=True)
-            lse_h.copy_(step.bufs["lse"], non_blocking=True)
-            e1.record(stream)
-            stream.synchronize()
-            if i > 0:                       # first pass warms the copy engines
-                times.append(e0.elapsed_time(e1))
-    ms = float(np.mean(times))
+    d2h = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * 4
+    dev = [{n: torch.empty_like(step.x[n]) for n in names} for _ in range(2)]
+    bufs = [step.bufs, api.alloc_prefill_outputs(step.shape, dev0, step.x["q"].dtype)]
+    s_in, s_out = torch.cuda.Stream(dev0), torch.cuda.Stream(dev0)
+    s_comp = stream
+
+    def run(n, pipelined):
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_comp = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(s_in)
+        for i in range(n):
+            j = i % 2 if pipelined else 0
+            with torch.cuda.stream(s_in):
+                if i >= 2 and pipelined:
+                    s_in.wait_event(ev_comp[i - 2])      # set j's inputs are consumed
+                if not pipelined and i >= 1:
+                    s_in.wait_event(ev_out[i - 1])
+                for nm in names:
+                    dev[j][nm].copy_(host[nm], non_blocking=True)
+                ev_in[i].record(s_in)
+            s_comp.wait_event(ev_in[i])
+            if i >= 2 and pipelined:
+                s_comp.wait_event(ev_out[i - 2])         # set j's outputs are read back
+            api.run_prefill(step.shape, dev[j]["q"], dev[j]["k"], dev[j]["v"], dev[j]["idx_q"],
+                            dev[j]["idx_k"], bufs[j], s_comp)
+            ev_comp[i].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                out_h[j].copy_(bufs[j]["out"], non_blocking=True)
+                lse_h[j].copy_(bufs[j]["lse"], non_blocking=True)
+                ev_out[i].record(s_out)
+        s_in.wait_event(ev_out[n - 1])
+        t1.record(s_in)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
+
+    run(2, True)                                       # warm the copy engines
+    ms = run(n_steps, True)
+    ms_serial = run(max(2, n_steps // 2), False)
     return {"value": cfg.seq * cfg.batch / (ms / 1e3), "unit": "tokens/s",
             "ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": n_steps}, host
+            "steps": n_steps, "pipelined": "copy-in / compute / copy-out on three streams",
+            "serial_value": cfg.seq * cfg.batch / (ms_serial / 1e3),
+            "serial_ms_per_step": ms_serial}, host
 
 
 def prefill_1m(args, device, stream, flush, tc_peak):
@@ -285,6 +319,46 @@ def prefill_1m(args, device, stream, flush, tc_peak):
     del step
     torch.cuda.empty_cache()
     return out
+
+
+def backward_32k(args, device, stream, flush, tc_peak):
+    """Training path: gradients of the sparse prefill attention at 32K context (CUDA cores;
+    reported against the same tensor peak as the forward, which it does not use)."""
+    cfg = CONFIGS["p32k"]
+    step = Step(cfg, device)
+    step.run(stream, False)
+    x, b = step.x, step.bufs
+    gen = torch.Generator(device=device).manual_seed(5)
+    dout = torch.randn(x["q"].shape, generator=gen, device=device).to(x["q"].dtype)
+    dq = torch.empty(x["q"].shape, device=device)
+    dk = torch.empty(x["k"].shape, device=device)
+    dv = torch.empty(x["v"].shape, device=device)
+
+    def run():
+        _lib.msa_sparse_prefill_backward(step.shape, x["q"], x["k"], x["v"], b["sel"], b["out"],
+                                         b["lse"], dout, dq, dk, dv, stream)
+    for _ in range(2):
+        run()
+    ts = []
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        stream.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    _lib.msa_get_device_status(stream)
+    ms = float(np.median(ts))
+    _, f_sparse, _ = prefill_flops(cfg)
+    f_bwd = f_sparse * 2.5          # Q.K^T, dout.V^T, dQ, dK, dV: 10 d per (row, key)
+    del step
+    torch.cuda.empty_cache()
+    return {"workload": f"{cfg.name}: {cfg.description}", "ms": ms,
+            "algorithmic_flops": f_bwd, "tflops": f_bwd / (ms / 1e3) / 1e12,
+            "frac_of_tensor_peak": f_bwd / (ms / 1e3) / 1e12 / tc_peak,
+            "kernel": "CUDA cores, fp32, dK/dV by fp32 atomics"}
 
 
 def cpu_baseline_prefill(cfg, host, budget_s=15.0, seed=0):
@@ -412,8 +486,10 @@ def run_ours(args, rank, world, device):
         }
     if not args.no_1m and pcfg.name != "p1m":
         line["prefill_1m"] = prefill_1m(args, device, stream, flush, tc_peak)
+    if not args.no_backward:
+        line["backward_32k"] = backward_32k(args, device, stream, flush, tc_peak)
     if not args.no_e2e:
-        e2e, host = e2e_prefill(pcfg, pre, stream, max(2, min(args.steps, 5)))
+        e2e, host = e2e_prefill(pcfg, pre, stream, max(4, min(args.steps, 8)))
         line["e2e"] = e2e
     else:
         host = {n: pre.x[n].cpu() for n in ["q", "k", "v", "idx_q", "idx_k"]}
@@ -545,6 +621,8 @@ def main(argv=None):
     ap.add_argument("--no-1m", action="store_true",
                     help="skip the secondary 1M-context prefill measurement")
     ap.add_argument("--steps-1m", type=int, default=3)
+    ap.add_argument("--no-backward", action="store_true",
+                    help="skip the training-path (backward) measurement")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

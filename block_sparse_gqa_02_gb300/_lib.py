@@ -45,6 +45,9 @@ SIGNATURES = {
     "msa_block_topk_shared": (_i32, [_SHAPE_P, _vp, _vp, _vp]),
     "msa_sparse_prefill": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "msa_sparse_prefill_backward": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                           _vp, _vp, _vp]),
+    "msa_index_kl_loss": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "msa_sparse_decode_static": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "msa_index_scores_paged": (_i32, [_SHAPE_P, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "msa_block_topk_ragged": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp]),
@@ -164,6 +167,22 @@ def msa_sparse_prefill(shape: MsaShape, q, k, v, sel, out, lse=None, workspace=N
     _check(load().msa_sparse_prefill(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(sel),
                                      _ptr(out), _ptr(lse), _ptr(workspace), ws_bytes,
                                      _stream(stream)), "msa_sparse_prefill")
+
+
+def msa_sparse_prefill_backward(shape: MsaShape, q, k, v, sel, out, lse, dout, dq, dk, dv,
+                                stream=None):
+    _check(load().msa_sparse_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                              _ptr(sel), _ptr(out), _ptr(lse), _ptr(dout),
+                                              _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
+           "msa_sparse_prefill_backward")
+
+
+def msa_index_kl_loss(shape: MsaShape, q, k, lse, idx_q, idx_k, sel, loss, d_idx_q, d_idx_k,
+                      stream=None):
+    _check(load().msa_index_kl_loss(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(lse),
+                                    _ptr(idx_q), _ptr(idx_k), _ptr(sel), _ptr(loss),
+                                    _ptr(d_idx_q), _ptr(d_idx_k), _stream(stream)),
+           "msa_index_kl_loss")
 
 
 def msa_sparse_decode(shape: MsaShape, q, k_cache, v_cache, sel, out, lse=None, workspace=None,

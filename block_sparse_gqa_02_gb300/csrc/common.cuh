@@ -84,6 +84,20 @@ cudaError_t launch_sparse_decode(const Dims& p, const void* q, const void* k, co
                                  const int32_t* sel, void* out, float* lse, float* ws,
                                  cudaStream_t st, int* dev_status);
 
+// Gradients of the sparse prefill attention: dq [B,Sq,Hq,d], dk, dv [B,Hkv,Sk,d], fp32;
+// dk and dv are cleared on the stream first, then accumulated.
+cudaError_t launch_sparse_prefill_backward(const Dims& p, const void* q, const void* k,
+                                           const void* v, const int32_t* sel, const void* out,
+                                           const float* lse, const void* dout, float* dq,
+                                           float* dk, float* dv, cudaStream_t st);
+
+// KL loss of the index branch toward the main branch (see index_kl.cu): loss (device
+// scalar, cleared then accumulated), d_idx_q [B,Sq,Hkv,dI] written, d_idx_k [B,Sk,dI]
+// cleared then accumulated; fp32.
+cudaError_t launch_index_kl(const Dims& p, const void* q, const void* k, const float* lse,
+                            const void* idx_q, const void* idx_k, const int32_t* sel,
+                            float* loss, float* d_idx_q, float* d_idx_k, cudaStream_t st);
+
 // Decode split-KV: number of block groups each (sequence, KV head) is split into, and
 // the scratch it needs (partial outputs and partial log-sum-exps, fp32).
 int decode_num_splits(const Dims& p);

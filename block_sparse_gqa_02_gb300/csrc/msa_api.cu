@@ -208,6 +208,54 @@ msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void*
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_prefill launch");
 }
 
+msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, const void* k,
+                                       const void* v, const int32_t* sel, const void* out,
+                                       const float* lse, const void* dout, float* dq, float* dk,
+                                       float* dv, void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  if (d.decode && d.Sk != 1)
+    return fail(MSA_ERR_INVALID_ARG, "msa_sparse_prefill_backward needs seq_q == seq_k");
+  MSA_TRY(check_ptr(q, "q"));
+  MSA_TRY(check_ptr(k, "k"));
+  MSA_TRY(check_ptr(v, "v"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  MSA_TRY(check_ptr(out, "out"));
+  MSA_TRY(check_ptr(lse, "lse"));
+  MSA_TRY(check_ptr(dout, "dout"));
+  MSA_TRY(check_ptr(dq, "dq"));
+  MSA_TRY(check_ptr(dk, "dk"));
+  MSA_TRY(check_ptr(dv, "dv"));
+  cudaError_t e = launch_sparse_prefill_backward(d, q, k, v, sel, out, lse, dout, dq, dk, dv,
+                                                 (cudaStream_t)stream);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_prefill_backward launch");
+}
+
+msa_status msa_index_kl_loss(const msa_shape* shape, const void* q, const void* k,
+                             const float* lse, const void* idx_q, const void* idx_k,
+                             const int32_t* sel, float* loss, float* d_idx_q, float* d_idx_k,
+                             void* stream) {
+  g_last_error[0] = 0;
+  Dims d;
+  MSA_TRY(make_dims(shape, &d));
+  if (d.decode && d.Sk != 1)
+    return fail(MSA_ERR_INVALID_ARG, "msa_index_kl_loss needs seq_q == seq_k");
+  if (d.G > 64) return fail(MSA_ERR_UNSUPPORTED, "index KL needs n_heads_q / n_heads_kv <= 64");
+  MSA_TRY(check_ptr(q, "q"));
+  MSA_TRY(check_ptr(k, "k"));
+  MSA_TRY(check_ptr(lse, "lse"));
+  MSA_TRY(check_ptr(idx_q, "idx_q"));
+  MSA_TRY(check_ptr(idx_k, "idx_k"));
+  MSA_TRY(check_ptr(sel, "sel"));
+  MSA_TRY(check_ptr(loss, "loss"));
+  MSA_TRY(check_ptr(d_idx_q, "d_idx_q"));
+  MSA_TRY(check_ptr(d_idx_k, "d_idx_k"));
+  cudaError_t e = launch_index_kl(d, q, k, lse, idx_q, idx_k, sel, loss, d_idx_q, d_idx_k,
+                                  (cudaStream_t)stream);
+  return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_kl_loss launch");
+}
+
 msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* k_cache,
                              const void* v_cache, const int32_t* sel, void* out, float* lse,
                              void* workspace, size_t ws_bytes, void* stream) {

@@ -127,6 +127,34 @@ msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void*
                               const void* v, const int32_t* sel, void* out, float* lse,
                               void* workspace, size_t ws_bytes, void* stream);
 
+/* Training: gradients of msa_sparse_prefill for a loss L with dL/dout = dout.  Inputs are
+ * the forward's q, k, v, sel, its out (dtype) and lse (natural log), and dout (dtype, same
+ * layout as out).  Outputs, float32: dq [batch, seq_q, n_heads_q, head_dim] (written),
+ * dk and dv [batch, n_heads_kv, seq_k, head_dim] (cleared on the stream, then accumulated:
+ * a key block selected by several tiles collects all their contributions).  With p the
+ * attention weights, D = dout . out, ds = p (dout . v - D): dq = sm_scale sum ds k,
+ * dk += sm_scale ds q, dv += p dout.  CUDA cores, fp32. */
+msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, const void* k,
+                                       const void* v, const int32_t* sel, const void* out,
+                                       const float* lse, const void* dout, float* dq, float* dk,
+                                       float* dv, void* stream);
+
+/* Training the index branch (the pages: the index branch is trained with a KL loss to match
+ * the main branch's attention).  The pages give no formula; this library's reading: for
+ * token t and KV head g, over the keys J the main branch attends (selected blocks, j <= t),
+ * the target is the main branch's attention distribution averaged over the group's query
+ * heads (held constant; computed from q, k and the forward's lse), the index distribution
+ * is the softmax over J of index_scale <idx_q[t,g], idx_k[j]>, and
+ *   loss = sum over (t, g) of KL(target || index)          (natural log).
+ * Outputs, float32: loss (one device scalar, cleared then accumulated), d_idx_q [batch,
+ * seq_q, n_heads_kv, index_dim] (written), d_idx_k [batch, seq_k, index_dim] (cleared, then
+ * accumulated over every tile and head): the gradients of loss.  Prefill shapes, at most
+ * 64 query heads per KV head.  CUDA cores, fp32. */
+msa_status msa_index_kl_loss(const msa_shape* shape, const void* q, const void* k,
+                             const float* lse, const void* idx_q, const void* idx_k,
+                             const int32_t* sel, float* loss, float* d_idx_q, float* d_idx_k,
+                             void* stream);
+
 /* Main branch, decode (seq_q == 1, q_tile == 1): the new token of every sequence attends
  * over the selected blocks of the cache (split over the blocks, partial results merged by
  * log-sum-exp).  workspace: device scratch of at least msa_workspace_bytes(shape, 1)

@@ -402,3 +402,117 @@ def block_topk_shared_prefill(scores, seq_len, q_tile, block_size, top_k):
     one = block_topk_prefill(agg[:, None].astype(np.float64), seq_len, q_tile, block_size,
                              top_k)
     return np.repeat(one, NI, axis=1)
+
+
+# ---------------------------------------------------------------------------
+# Training: gradients of the sparse attention (the main branch's backward pass)
+# ---------------------------------------------------------------------------
+
+def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=None):
+    """Gradients of L = sum(dout * out) for out = sparse_attention(q, k, v, sel, ...) (prefill).
+
+    With z_j = sm_scale q.k_j over the row's keys J (selected blocks, j <= t),
+    p = softmax(z), out = sum_j p_j v_j and D = dout . out:
+      dv_j += p_j dout,   dp_j = dout . v_j,   ds_j = p_j (dp_j - D),
+      dq    = sm_scale sum_j ds_j k_j,        dk_j += sm_scale ds_j q.
+    A key block selected by several tiles collects the contributions of all of them.
+    Returns (dq [B,T,Hq,d], dk [B,Hkv,T,d], dv [B,Hkv,T,d]) in float64.
+    """
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    if sm_scale is None or sm_scale == 0:
+        sm_scale = default_scale(d)
+    dq = np.zeros((B, T, Hq, d))
+    dk = np.zeros((B, Hkv, T, d))
+    dv = np.zeros((B, Hkv, T, d))
+    nT = -(-T // q_tile)
+    for m in range(nT):
+        t_idx = np.arange(m * q_tile, min(T, (m + 1) * q_tile))
+        for b in range(B):
+            for g in range(Hkv):
+                J = selected_keys(sel[b, g, m], block_size, T)
+                if J.size == 0:
+                    continue
+                hs = slice(g * G, (g + 1) * G)
+                qr = _rows(q, b, slice(int(t_idx[0]), int(t_idx[-1]) + 1), hs)     # [n, G, d]
+                dor = _rows(dout, b, slice(int(t_idx[0]), int(t_idx[-1]) + 1), hs)
+                kj, vj = _rows(k, b, g, J), _rows(v, b, g, J)                      # [|J|, d]
+                z = sm_scale * np.matmul(qr, kj.T)                                 # [n, G, |J|]
+                z = np.where(J[None, None, :] <= t_idx[:, None, None], z, -np.inf)
+                zmax = z.max(axis=2, keepdims=True)
+                zmax = np.where(np.isfinite(zmax), zmax, 0.0)
+                e = np.exp(z - zmax)
+                ssum = e.sum(axis=2, keepdims=True)
+                p = np.where(ssum > 0, e / np.where(ssum > 0, ssum, 1.0), 0.0)
+                o = np.matmul(p, vj)                                               # [n, G, d]
+                D = (dor * o).sum(axis=2, keepdims=True)                           # [n, G, 1]
+                dp = np.matmul(dor, vj.T)                                          # [n, G, |J|]
+                ds = p * (dp - D)
+                dq[b, t_idx, hs] += sm_scale * np.matmul(ds, kj)
+                dk[b, g, J] += sm_scale * np.einsum("ngj,ngc->jc", ds, qr)
+                dv[b, g, J] += np.einsum("ngj,ngc->jc", p, dor)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Training the index branch: KL to the main branch's attention
+# ---------------------------------------------------------------------------
+
+def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
+                  index_scale=None):
+    """KL loss that trains the index branch toward the main branch's attention ("Sparse
+    Attention Cannot Be Directly Ported Across Architectures", paragraph introducing MSA;
+    aietalks.com, "MSA uses a lightweight index branch before sparse attention": the index
+    branch is trained with a KL loss to match the main branch's attention scores).
+
+    Reading taken (the pages give no formula): for token t and KV head g, over the keys J the
+    main branch attends (selected blocks, j <= t), the target is the main branch's attention
+    distribution averaged over the group's G query heads, held constant; the index
+    distribution is the softmax over J of the index logits index_scale <idx_q[t,g], idx_k[j]>;
+    the loss is sum over (t, g) of KL(target || index).  Returns (loss, d idx_q, d idx_k) in
+    float64, the gradients being those of the summed loss.
+    """
+    B, T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    dI = idx_q.shape[-1]
+    if sm_scale is None or sm_scale == 0:
+        sm_scale = default_scale(d)
+    if index_scale is None or index_scale == 0:
+        index_scale = default_scale(dI)
+    loss = 0.0
+    diq = np.zeros((B, T, Hkv, dI))
+    dik = np.zeros((B, T, dI))
+    nT = -(-T // q_tile)
+    for m in range(nT):
+        t_idx = np.arange(m * q_tile, min(T, (m + 1) * q_tile))
+        ts = slice(int(t_idx[0]), int(t_idx[-1]) + 1)
+        for b in range(B):
+            for g in range(Hkv):
+                J = selected_keys(sel[b, g, m], block_size, T)
+                if J.size == 0:
+                    continue
+                vis = J[None, :] <= t_idx[:, None]                                 # [n, |J|]
+                # target: main attention over J, averaged over the group's heads
+                z = sm_scale * np.matmul(_rows(q, b, ts, slice(g * G, (g + 1) * G)),
+                                         _rows(k, b, g, J).T)                      # [n, G, |J|]
+                z = np.where(vis[:, None, :], z, -np.inf)
+                z = z - z.max(axis=2, keepdims=True)
+                pm = np.exp(z)
+                pm = pm / pm.sum(axis=2, keepdims=True)
+                target = pm.mean(axis=1)                                           # [n, |J|]
+                # index distribution over the same keys
+                qi = _rows(idx_q, b, ts, g)                                        # [n, dI]
+                ki = _rows(idx_k, b, J)                                            # [|J|, dI]
+                s = np.where(vis, index_scale * np.matmul(qi, ki.T), -np.inf)
+                s = s - s.max(axis=1, keepdims=True)
+                log_pi = s - np.log(np.exp(s).sum(axis=1, keepdims=True))
+                pi = np.exp(log_pi)
+                with np.errstate(divide="ignore", invalid="ignore"):
+                    terms = np.where(target > 0, target * (np.log(target) - log_pi), 0.0)
+                loss += float(terms.sum())
+                gs = np.where(vis, pi - target, 0.0)                               # dL/ds
+                diq[b, ts, g] += index_scale * np.matmul(gs, ki)
+                dik[b, J] += index_scale * np.matmul(gs.T, qi)
+    return loss, diq, dik

@@ -430,10 +430,123 @@ def pin_paged_equals_contiguous(o):
         assert np.allclose(lse[b], lse1[0], rtol=1e-13, atol=1e-13)
 
 
+def pin_backward_finite_differences(o):
+    """Sparse-attention gradients against central finite differences of sum(dout * out)."""
+    r = _rng(31)
+    B, T, Hq, Hkv, d, bs, qt, kk = 1, 12, 4, 2, 3, 4, 2, 2
+    q, k, v = (r.standard_normal((B, T, Hq, d)), r.standard_normal((B, Hkv, T, d)),
+               r.standard_normal((B, Hkv, T, d)))
+    dout = r.standard_normal((B, T, Hq, d))
+    sel = _random_sel(o, T, qt, bs, kk, Hkv, 32)
+    dq, dk, dv = o.sparse_attention_backward(q, k, v, sel, dout, bs, qt, 0.8)
+
+    def loss(q_, k_, v_):
+        out, _ = o.sparse_attention(q_, k_, v_, sel, bs, qt, 0.8)
+        return float((dout * out).sum())
+    h = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for _ in range(12):
+            idx = tuple(int(r.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args = {"q": (q, k, v), "k": (q, k, v), "v": (q, k, v)}[name]
+            fp = loss(*[xp if a is x else a for a in args])
+            fm = loss(*[xm if a is x else a for a in args])
+            num = (fp - fm) / (2 * h)
+            assert abs(num - grad[idx]) <= 1e-6 * max(1.0, abs(num)), (name, idx, num, grad[idx])
+
+
+def pin_backward_full_k_autograd(o):
+    """k = all blocks: the gradients equal torch autograd of causal GQA SDPA in float64."""
+    import torch
+    r = _rng(33)
+    B, T, Hq, Hkv, d, bs, qt = 1, 40, 8, 2, 8, 8, 4
+    q = r.standard_normal((B, T, Hq, d))
+    k = r.standard_normal((B, Hkv, T, d))
+    v = r.standard_normal((B, Hkv, T, d))
+    dout = r.standard_normal((B, T, Hq, d))
+    nT, nB = T // qt, T // bs
+    sel = o.block_topk_prefill(r.standard_normal((B, Hkv, nT, nB)), T, qt, bs, nB)
+    dq, dk, dv = o.sparse_attention_backward(q, k, v, sel, dout, bs, qt, None)
+    tq = torch.from_numpy(q).permute(0, 2, 1, 3).requires_grad_()
+    tk = torch.from_numpy(k).requires_grad_()
+    tv = torch.from_numpy(v).requires_grad_()
+    out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True,
+                                                           enable_gqa=True)
+    out.backward(torch.from_numpy(dout).permute(0, 2, 1, 3))
+    assert np.allclose(dq, tq.grad.permute(0, 2, 1, 3).numpy(), rtol=1e-9, atol=1e-10)
+    assert np.allclose(dk, tk.grad.numpy(), rtol=1e-9, atol=1e-10)
+    assert np.allclose(dv, tv.grad.numpy(), rtol=1e-9, atol=1e-10)
+
+
+def pin_index_kl(o):
+    """KL of the index branch: zero with zero gradient when the index branch is the main
+    branch (G = 1, same queries, keys and scale); positive otherwise, with gradients equal
+    to central finite differences."""
+    r = _rng(41)
+    B, T, Hkv, d, bs, qt, kk = 1, 16, 2, 4, 4, 2, 3
+    q = r.standard_normal((B, T, Hkv, d))                 # G = 1
+    k = r.standard_normal((B, Hkv, T, d))
+    sel = _random_sel(o, T, qt, bs, kk, Hkv, 42)
+    # index keys are shared by the KV heads: use one KV head's keys for both heads' test
+    k_shared = np.repeat(k[:, :1], Hkv, axis=1)
+    loss0, gq0, gk0 = o.index_kl_loss(q, k_shared, q, k_shared[:, 0], sel, bs, qt, 0.5, 0.5)
+    assert abs(loss0) < 1e-12 and np.abs(gq0).max() < 1e-12 and np.abs(gk0).max() < 1e-12
+    iq = r.standard_normal((B, T, Hkv, 3))
+    ik = r.standard_normal((B, T, 3))
+    loss, gq, gk = o.index_kl_loss(q, k, iq, ik, sel, bs, qt, 0.5, 0.7)
+    assert loss > 0
+    h = 1e-6
+    for name, x, grad in (("iq", iq, gq), ("ik", ik, gk)):
+        for _ in range(10):
+            idx = tuple(int(r.integers(0, n)) for n in x.shape)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            if name == "iq":
+                fp = o.index_kl_loss(q, k, xp, ik, sel, bs, qt, 0.5, 0.7)[0]
+                fm = o.index_kl_loss(q, k, xm, ik, sel, bs, qt, 0.5, 0.7)[0]
+            else:
+                fp = o.index_kl_loss(q, k, iq, xp, sel, bs, qt, 0.5, 0.7)[0]
+                fm = o.index_kl_loss(q, k, iq, xm, sel, bs, qt, 0.5, 0.7)[0]
+            num = (fp - fm) / (2 * h)
+            assert abs(num - grad[idx]) <= 1e-6 * max(1.0, abs(num)), (name, idx, num, grad[idx])
+
+
+def pin_index_kl_group_mean(o):
+    """KL with G = 2 query heads per KV head against a plain-loop restatement: per (token,
+    KV head), each head's softmax over the visible selected keys, their mean as the target,
+    the index softmax, and scipy's relative entropy of the two."""
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    r = _rng(43)
+    B, T, Hkv, G, d, dI, bs, qt, kk = 1, 14, 2, 2, 3, 2, 3, 2, 2
+    q = r.standard_normal((B, T, Hkv * G, d))
+    k = r.standard_normal((B, Hkv, T, d))
+    iq = r.standard_normal((B, T, Hkv, dI))
+    ik = r.standard_normal((B, T, dI))
+    sel = _random_sel(o, T, qt, bs, kk, Hkv, 44)
+    loss = o.index_kl_loss(q, k, iq, ik, sel, bs, qt, 0.9, 0.6)[0]
+    ref = 0.0
+    for t in range(T):
+        for g in range(Hkv):
+            J = [j for blk in sel[0, g, t // qt] if blk >= 0
+                 for j in range(blk * bs, min(T, (blk + 1) * bs)) if j <= t]
+            heads = [softmax([0.9 * sum(q[0, t, g * G + hh, c] * k[0, g, j, c] for c in range(d))
+                              for j in J]) for hh in range(G)]
+            target = [sum(hp[i] for hp in heads) / G for i in range(len(J))]
+            index = softmax([0.6 * sum(iq[0, t, g, c] * ik[0, j, c] for c in range(dI))
+                             for j in J])
+            ref += entropy(target, index)
+    assert abs(loss - ref) <= 1e-10 * max(1.0, abs(ref)), (loss, ref)
+
+
 ALL_PINS = [
     pin_scores_block1_tile1, pin_scores_bruteforce, pin_decode_scores_bruteforce,
     pin_topk_bruteforce, pin_topk_layout, pin_full_k_bruteforce, pin_full_k_sdpa,
     pin_sparse_bruteforce, pin_rows_sum_to_one, pin_unselected_invariance,
     pin_decode_equals_prefill_row, pin_planted_selected, pin_head_diversity,
-    pin_worked_example, pin_paged_equals_contiguous,
+    pin_worked_example, pin_paged_equals_contiguous, pin_backward_finite_differences,
+    pin_backward_full_k_autograd, pin_index_kl, pin_index_kl_group_mean,
 ]

@@ -6,6 +6,9 @@ Tolerances (written here once, used by every parity test):
   max-abs <= 1e-4;
 * lse (natural log): |gpu - ref| <= 2e-3 for bf16 inputs, 1e-4 for fp32 -- fp32
   accumulation of exact bf16 products over <= 8192 keys;
+* gradients (dq, dk, dv of the sparse attention): rel-L2 <= 1e-4 for fp32 inputs; for bf16
+  rel-L2 <= 1e-2, because the backward uses the forward output rounded to bf16 in
+  D = dout . out (relative 2^-9 per element), and max-abs <= 5e-2 of the largest |ref|;
 * selections: bit-exact where both sides rank the same fp32 scores; where the oracle
   ranks its own fp64 scores, a differing choice must be one a score tolerance allows.
 """
@@ -73,6 +76,22 @@ def check_lse(gpu, ref, dtype, what="lse"):
     mx = float(err.max()) if err.size else 0.0
     assert mx <= LSE_TOL[dtype], f"{what}: max error {mx:.3g} > {LSE_TOL[dtype]}"
     return mx
+
+
+GRAD_TOL = {"bf16": (1e-2, 5e-2), "f32": (1e-4, 1e-3)}
+
+
+def check_grad(gpu, ref, dtype, what="grad"):
+    gpu, ref = to_np(gpu).astype(np.float64), np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    assert np.isfinite(gpu).all(), f"{what}: non-finite values"
+    diff = gpu - ref
+    rel = float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300))
+    mx = float(np.max(np.abs(diff)) / max(np.max(np.abs(ref)), 1e-300))
+    rtol, atol = GRAD_TOL[dtype]
+    assert rel <= rtol and mx <= atol, f"{what}: rel-L2 {rel:.3g} (<= {rtol}), " \
+        f"max-abs / max|ref| {mx:.3g} (<= {atol})"
+    return rel, mx
 
 
 def check_selection_valid(gpu_sel, ref_sel, ref_scores, cur_blocks, what="sel"):

@@ -1,0 +1,84 @@
+"""Gradients of the sparse prefill attention (training path) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_gqa_02_gb300 import _lib
+from block_sparse_gqa_02_gb300.configs import CONFIGS
+from block_sparse_gqa_02_gb300.inputs import make_inputs, random_selection
+from tests.parity import check_grad
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny_f32": CONFIGS["tiny"],
+    "f32_ragged_qt16": CONFIGS["tiny"].with_(seq=1000, q_tile=16, block_size=32, top_k=5),
+    "bf16_ragged_1000": CONFIGS["p32k"].with_(seq=1000, top_k=4, n_plants=0),
+    "bf16_d64_g16": CONFIGS["p32k"].with_(seq=2048, head_dim=64, n_heads_q=64, top_k=6),
+    "bf16_4096_k16": CONFIGS["p32k"].with_(seq=4096, n_plants=0),
+    "bf16_qt128_ragged": CONFIGS["p32k"].with_(seq=1500, q_tile=128, top_k=4, n_plants=0),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_sparse_prefill_backward(name):
+    cfg = CASES[name]
+    x = make_inputs(cfg, device="cuda")
+    shape = _lib.shape_from_config(cfg)
+    cur = np.array([min(cfg.seq - 1, m * cfg.q_tile + cfg.q_tile - 1) // cfg.block_size
+                    for m in range(shape.n_rows)])
+    sel_np = random_selection(np.broadcast_to(cur + 1, (1, 4, shape.n_rows)), cfg.top_k, 5)
+    sel = torch.from_numpy(sel_np).cuda()
+    gen = torch.Generator(device="cuda").manual_seed(99)
+    dout = torch.randn(x["q"].shape, generator=gen, device="cuda").to(x["q"].dtype)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((1, cfg.n_heads_q, cfg.seq), device="cuda")
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    dq = torch.full(x["q"].shape, float("nan"), device="cuda")
+    dk = torch.full(x["k"].shape, float("nan"), device="cuda")
+    dv = torch.full(x["v"].shape, float("nan"), device="cuda")
+    _lib.msa_sparse_prefill_backward(shape, x["q"], x["k"], x["v"], sel, out, lse, dout,
+                                     dq, dk, dv)
+    _lib.msa_get_device_status()
+    rq, rk, rv = oracle.sparse_attention_backward(x["q"], x["k"], x["v"], sel_np, dout,
+                                                  cfg.block_size, cfg.q_tile)
+    check_grad(dq, rq, cfg.dtype, f"{name} dq")
+    check_grad(dk, rk, cfg.dtype, f"{name} dk")
+    check_grad(dv, rv, cfg.dtype, f"{name} dv")
+
+
+KL_CASES = {
+    "tiny_f32": CONFIGS["tiny"],
+    "bf16_ragged_1000": CONFIGS["p32k"].with_(seq=1000, top_k=4, n_plants=3),
+    "bf16_d64_di64_g16": CONFIGS["p32k"].with_(seq=2048, head_dim=64, index_dim=64,
+                                               n_heads_q=64, top_k=6, block_size=64),
+    "bf16_4096_k16": CONFIGS["p32k"].with_(seq=4096, n_plants=5),
+    "bf16_qt128_ragged": CONFIGS["p32k"].with_(seq=1500, q_tile=128, top_k=4, n_plants=2),
+}
+
+
+@pytest.mark.parametrize("name", list(KL_CASES))
+def test_index_kl_loss(name):
+    cfg = KL_CASES[name]
+    x = make_inputs(cfg, device="cuda")
+    shape = _lib.shape_from_config(cfg)
+    cur = np.array([min(cfg.seq - 1, m * cfg.q_tile + cfg.q_tile - 1) // cfg.block_size
+                    for m in range(shape.n_rows)])
+    sel_np = random_selection(np.broadcast_to(cur + 1, (1, 4, shape.n_rows)), cfg.top_k, 6)
+    sel = torch.from_numpy(sel_np).cuda()
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((1, cfg.n_heads_q, cfg.seq), device="cuda")
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    loss = torch.full((1,), float("nan"), device="cuda")
+    diq = torch.full(x["idx_q"].shape, float("nan"), device="cuda")
+    dik = torch.full(x["idx_k"].shape, float("nan"), device="cuda")
+    _lib.msa_index_kl_loss(shape, x["q"], x["k"], lse, x["idx_q"], x["idx_k"], sel, loss,
+                           diq, dik)
+    _lib.msa_get_device_status()
+    ref_loss, ref_q, ref_k = oracle.index_kl_loss(x["q"], x["k"], x["idx_q"], x["idx_k"],
+                                                  sel_np, cfg.block_size, cfg.q_tile)
+    assert abs(loss.item() - ref_loss) <= 1e-3 * abs(ref_loss), (loss.item(), ref_loss)
+    tol = "f32" if cfg.dtype == "f32" else "bf16"
+    check_grad(diq, ref_q, tol, f"{name} d idx_q")
+    check_grad(dik, ref_k, tol, f"{name} d idx_k")

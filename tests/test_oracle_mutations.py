@@ -121,9 +121,40 @@ def _mut_transposed_index(o):
     o.index_logits = index_logits
 
 
+def _mut_backward_no_D(o):
+    # dq with ds = p * dp, the -D term of the softmax Jacobian dropped: that adds
+    # sm_scale * D * (sum_j p_j k_j), the attention output with v replaced by k
+    base = o.sparse_attention_backward
+
+    def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=None):
+        dq, dk, dv = base(q, k, v, sel, dout, block_size, q_tile, sm_scale)
+        out, _ = o.sparse_attention(q, k, v, sel, block_size, q_tile, sm_scale)
+        kbar, _ = o.sparse_attention(q, k, k, sel, block_size, q_tile, sm_scale)
+        scale = sm_scale if sm_scale else 1.0 / np.sqrt(np.asarray(q).shape[-1])
+        D = (np.asarray(dout, np.float64) * out).sum(-1, keepdims=True)
+        return dq + scale * D * kbar, dk, dv
+    o.sparse_attention_backward = sparse_attention_backward
+
+
+def _mut_kl_first_head_target(o):
+    # the target built from the group's first query head only instead of the mean
+    base = o.index_kl_loss
+
+    def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
+                      index_scale=None):
+        q = np.asarray(q, dtype=np.float64).copy()
+        Hq, Hkv = q.shape[2], np.asarray(k).shape[1]
+        G = Hq // Hkv
+        for g in range(Hkv):
+            q[:, :, g * G:(g + 1) * G] = q[:, :, g * G:g * G + 1]
+        return base(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale, index_scale)
+    o.index_kl_loss = index_kl_loss
+
+
 MUTATIONS = [_mut_strict_mask, _mut_no_index_scale, _mut_mean_pool, _mut_ties_high,
              _mut_no_forced_current, _mut_unsorted_output, _mut_current_block_first_query,
-             _mut_block_keys_short, _mut_strided_groups, _mut_transposed_index]
+             _mut_block_keys_short, _mut_strided_groups, _mut_transposed_index,
+             _mut_backward_no_D, _mut_kl_first_head_target]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__[5:] for m in MUTATIONS])
