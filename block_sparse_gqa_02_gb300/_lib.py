@@ -46,7 +46,7 @@ SIGNATURES = {
     "msa_sparse_prefill": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_decode": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_prefill_backward": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                           _vp, _vp, _vp]),
+                                           _vp, _vp, _vp, _sz, _vp]),
     "msa_index_kl_loss": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "msa_sparse_decode_static": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "msa_index_scores_paged": (_i32, [_SHAPE_P, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
@@ -170,10 +170,13 @@ def msa_sparse_prefill(shape: MsaShape, q, k, v, sel, out, lse=None, workspace=N
 
 
 def msa_sparse_prefill_backward(shape: MsaShape, q, k, v, sel, out, lse, dout, dq, dk, dv,
-                                stream=None):
+                                workspace=None, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().msa_sparse_prefill_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
                                               _ptr(sel), _ptr(out), _ptr(lse), _ptr(dout),
-                                              _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)),
+                                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                              ws_bytes, _stream(stream)),
            "msa_sparse_prefill_backward")
 
 

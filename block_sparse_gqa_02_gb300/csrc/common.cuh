@@ -89,7 +89,10 @@ cudaError_t launch_sparse_decode(const Dims& p, const void* q, const void* k, co
 cudaError_t launch_sparse_prefill_backward(const Dims& p, const void* q, const void* k,
                                            const void* v, const int32_t* sel, const void* out,
                                            const float* lse, const void* dout, float* dq,
-                                           float* dk, float* dv, cudaStream_t st);
+                                           float* dk, float* dv, void* workspace,
+                                           cudaStream_t st, int* status);
+// Workspace bytes of the backward (0 on the CUDA-core path).
+size_t backward_workspace_bytes(const Dims& p);
 
 // KL loss of the index branch toward the main branch (see index_kl.cu): loss (device
 // scalar, cleared then accumulated), d_idx_q [B,Sq,Hkv,dI] written, d_idx_k [B,Sk,dI]

@@ -211,7 +211,8 @@ msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void*
 msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, const void* k,
                                        const void* v, const int32_t* sel, const void* out,
                                        const float* lse, const void* dout, float* dq, float* dk,
-                                       float* dv, void* stream) {
+                                       float* dv, void* workspace, size_t ws_bytes,
+                                       void* stream) {
   g_last_error[0] = 0;
   Dims d;
   MSA_TRY(make_dims(shape, &d));
@@ -227,8 +228,14 @@ msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, co
   MSA_TRY(check_ptr(dq, "dq"));
   MSA_TRY(check_ptr(dk, "dk"));
   MSA_TRY(check_ptr(dv, "dv"));
+  const size_t need = backward_workspace_bytes(d);
+  if (need > 0) {
+    MSA_TRY(check_ptr(workspace, "workspace"));
+    if (ws_bytes < need)
+      return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  }
   cudaError_t e = launch_sparse_prefill_backward(d, q, k, v, sel, out, lse, dout, dq, dk, dv,
-                                                 (cudaStream_t)stream);
+                                                 workspace, (cudaStream_t)stream, status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_prefill_backward launch");
 }
 
@@ -363,6 +370,7 @@ size_t msa_workspace_bytes(const msa_shape* shape, int which) {
   Dims d;
   if (make_dims(shape, &d) != MSA_OK) return 0;
   if (which == 1 && d.decode) return decode_workspace_bytes(d);
+  if (which == 2 && !d.decode) return backward_workspace_bytes(d);
   return 0;
 }
 

@@ -61,7 +61,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with the given parity to complete.  Gives up after
 // `limit_ns` (or as soon as *abort is set by another thread) and returns false; the
-// caller then records the failure and winds down instead of hanging.
+// caller then records the failure and winds down instead of hanging.  Called by all 32
+// lanes of a converged warp: the lanes read the barrier, the abort flag and the timer in
+// the same instructions, so they leave together with the same result and the warp stays
+// converged for the warp-collective tcgen05.ld/st, ldmatrix and mma.sync that follow.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // one second
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,

@@ -255,9 +255,11 @@ cudaError_t decode_split(const Dims& p, const void* q, const void* k, const void
 }  // namespace
 
 int decode_num_splits(const Dims& p) {
-  // enough CTAs to cover the GPU a few times over, never more splits than blocks
+  // one wave of CTAs over the 152 SMs (one resident CTA per SM): each CTA then streams a
+  // long run of blocks through its TMA ring instead of paying the ring's fill and drain
+  // several times; never more splits than blocks
   const int units = p.B * p.Hkv;
-  int s = (4 * 152 + units - 1) / units;
+  int s = 152 / units;
   if (s > p.k) s = p.k;
   if (s < 1) s = 1;
   return s;

@@ -14,6 +14,7 @@
 // that selected it.  CUDA cores, fp32 throughout; a first implementation of the training
 // path (the tensor-core forward kernels are the optimised hot path).
 #include "common.cuh"
+#include "sparse_backward_tc.cuh"
 
 namespace msa {
 
@@ -198,12 +199,20 @@ cudaError_t backward(const Dims& p, const void* q, const void* k, const void* v,
 cudaError_t launch_sparse_prefill_backward(const Dims& p, const void* q, const void* k,
                                            const void* v, const int32_t* sel, const void* out,
                                            const float* lse, const void* dout, float* dq,
-                                           float* dk, float* dv, cudaStream_t st) {
+                                           float* dk, float* dv, void* workspace,
+                                           cudaStream_t st, int* status) {
+  if (sparse_backward_tc_supported(p))
+    return launch_sparse_backward_tc(p, q, k, v, sel, out, lse, dout, dq, dk, dv, workspace, st,
+                                     status);
   if (p.dtype == 1)
     return p.d == 128 ? backward<__nv_bfloat16, 128>(p, q, k, v, sel, out, lse, dout, dq, dk, dv, st)
                       : backward<__nv_bfloat16, 64>(p, q, k, v, sel, out, lse, dout, dq, dk, dv, st);
   return p.d == 128 ? backward<float, 128>(p, q, k, v, sel, out, lse, dout, dq, dk, dv, st)
                     : backward<float, 64>(p, q, k, v, sel, out, lse, dout, dq, dk, dv, st);
+}
+
+size_t backward_workspace_bytes(const Dims& p) {
+  return sparse_backward_tc_supported(p) ? sparse_backward_tc_workspace_bytes(p) : 0;
 }
 
 }  // namespace msa

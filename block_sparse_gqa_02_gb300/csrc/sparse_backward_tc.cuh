@@ -1,0 +1,14 @@
+// tcgen05 backward of the sparse prefill attention (bf16, head_dim 128, block 128, 64-query
+// tiles): a dQ kernel over query tiles and a dK/dV kernel over key blocks.
+#pragma once
+#include "common.cuh"
+
+namespace msa {
+bool sparse_backward_tc_supported(const Dims& p);
+// scratch: D = dout . out per row [B, Hq, Sq] fp32, then the tile-selects-block bitmap
+size_t sparse_backward_tc_workspace_bytes(const Dims& p);
+cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* k,
+                                      const void* v, const int32_t* sel, const void* out,
+                                      const float* lse, const void* dout, float* dq, float* dk,
+                                      float* dv, void* workspace, cudaStream_t st, int* status);
+}  // namespace msa

@@ -31,13 +31,18 @@ constexpr int kThreads = (kComputeWarps + 1) * 32;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// The warps' partial outputs reuse the K/V ring once every copy into it has landed.
 struct __align__(1024) Smem {
-  uint8_t k[kStages][kBlockBytes];
-  uint8_t v[kStages][kBlockBytes];
+  union {
+    struct {
+      uint8_t k[kStages][kBlockBytes];
+      uint8_t v[kStages][kBlockBytes];
+    };
+    float o[kComputeWarps][16][kD + 4];
+  };
   uint64_t full[kStages], empty[kStages];
   float m[kComputeWarps][16];
   float l[kComputeWarps][16];
-  float o[kComputeWarps][16][kD + 4];
   int abort;
 };
 
@@ -111,6 +116,12 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
   auto block_at = [&](int i) { return srow[i]; };
   auto valid = [&](int blk) { return blk >= 0 && blk < nB_b; };
 
+  // a compute warp's running output, row maxima and row sums (rows gr and gr + 8)
+  float o[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
   if (warp == kComputeWarps) {
     // ------------------------------------------------------------- TMA producer
     int j = 0;
@@ -159,10 +170,6 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
         qa[kk][3] = gr + 8 < G ? q1[kk * 8 + 4 + c] : 0u;
       }
     }
-    float o[16][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
     bool ok = true;
     int j = 0;
     for (int i = i0; i < i1; ++i) {
@@ -247,6 +254,11 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
       s.abort = 1;
       if (status) atomicExch(status, 0x402);
     }
+  }
+  // every copy into the ring has landed (the producer drained any in flight on abort)
+  __syncthreads();
+  if (warp < kComputeWarps) {
+    const int gr = lane >> 2, c = lane & 3;
     // this warp's partial state -> shared memory (row sums reduced over the quad)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {

@@ -322,64 +322,36 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ptx::mbar_wait(&s.s_full[i], j & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) ptx::tmem_ld_x32(s_addr + c * 32, sv[c]);
-      ptx::tmem_ld_wait();
       // keys j > t are masked; only a block reaching past this row's token needs it
       const int lim = t - blk * kBk;                         // visible columns: c <= lim
-      // four independent max chains (one per 32-column chunk) keep the dependency short
-      float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (lim >= kBk - 1) {
+      const uint64_t c1x2 = f32x2(c1, c1);
+      // P = 2^(s * c1 - base) from the S values in sv, written over S as bf16; returns the
+      // row sum of P.  Pairs of columns go through packed fp32 FMA / ADD, with one sum chain
+      // per 32-column chunk.
+      auto p_from_sv = [&](float base) {
+        const uint64_t negm = f32x2(-base, -base);
+        uint64_t acc[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+          acc[c] = f32x2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 32; e += 2)
-            mc[c] = max3(mc[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
-      } else {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float x = c * 32 + e <= lim ? __uint_as_float(sv[c][e]) : -INFINITY;
-            sv[c][e] = __float_as_uint(x);
-            mc[c] = fmaxf(mc[c], x);
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t y = fma_f32x2(
+                f32x2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])), c1x2, negm);
+            const float p0 = ex2(lo_f32(y)), p1 = ex2(hi_f32(y));
+            acc[c] = add_f32x2(acc[c], f32x2(p0, p1));
+            pk[e >> 1] = pack_bf16x2(p0, p1);
           }
-      }
-      const float mx = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
-      const float mb = mx * c1;                              // block max, log2 units
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mb > m_used + kRescaleThreshold) {
-        if (m_used != -INFINITY) {
-          alpha = ex2(m_used - mb);
-          rescale = true;
-          l *= alpha;
+          ptx::tmem_st_x16(s_addr + c * 16, pk);
         }
-        m_used = mb;
-      }
-      const float m_eff = m_used == -INFINITY ? 0.f : m_used;
-      // p = 2^(s * c1 - m): pairs of columns through packed fp32 FMA / ADD
-      const uint64_t c1x2 = f32x2(c1, c1), negm = f32x2(-m_eff, -m_eff);
-      uint64_t acc[4];                                       // one sum chain per chunk
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-        acc[c] = f32x2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const uint64_t y = fma_f32x2(f32x2(__uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1])),
-                                       c1x2, negm);
-          const float p0 = ex2(lo_f32(y)), p1 = ex2(hi_f32(y));
-          acc[c] = add_f32x2(acc[c], f32x2(p0, p1));
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-        }
-        ptx::tmem_st_x16(s_addr + c * 16, pk);
-      }
-      const uint64_t accs = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
-      l += lo_f32(accs) + hi_f32(accs);
-      if (rescale) {
-        // P.V of the previous block is complete (it precedes this block's Q.K^T); O is
-        // rescaled before this block's P is released to the MMA warp
+        const uint64_t accs = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
+        return lo_f32(accs) + hi_f32(accs);
+      };
+      // O *= alpha in every row of the warp (alpha = 1 in rows that keep their base).  The
+      // P.V of the previous block is complete (it precedes this block's Q.K^T), and O is
+      // rescaled before this block's P is released to the MMA warp.
+      auto rescale_o = [&](float alpha) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
@@ -389,6 +361,88 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
           ptx::tmem_st_x32(o_addr + c * 32, ov);
         }
+      };
+      // tcgen05.ld/st are warp-collective, so every branch around them is warp-uniform.
+      if (__all_sync(0xffffffffu, m_used != -INFINITY && lim >= kBk - 1)) {
+        // A later block with no masked key: P is formed with the running base while S
+        // streams in from TMEM a chunk at a time (the next chunk loads while this one is
+        // exponentiated), and the block's maximum is checked afterwards.  P chunk c lands on
+        // S columns 16c .. 16c+15, which were loaded before.
+        const uint64_t negm = f32x2(-m_used, -m_used);
+        float mc[4];
+        uint64_t acc[4];
+        ptx::tmem_ld_x32(s_addr, sv[0]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (c < 3) ptx::tmem_ld_x32(s_addr + (c + 1) * 32, sv[c + 1]);
+          uint32_t pk[16];
+          mc[c] = -INFINITY;
+          acc[c] = f32x2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float x0 = __uint_as_float(sv[c][e]), x1 = __uint_as_float(sv[c][e + 1]);
+            mc[c] = max3(mc[c], x0, x1);
+            const uint64_t y = fma_f32x2(f32x2(x0, x1), c1x2, negm);
+            const float p0 = ex2(lo_f32(y)), p1 = ex2(hi_f32(y));
+            acc[c] = add_f32x2(acc[c], f32x2(p0, p1));
+            pk[e >> 1] = pack_bf16x2(p0, p1);
+          }
+          ptx::tmem_st_x16(s_addr + c * 16, pk);
+          if (c < 3) ptx::tmem_ld_wait();
+        }
+        const float mb = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c1;
+        const bool redo = mb > m_used + kRescaleThreshold;
+        float alpha = 1.f;
+        if (redo) {
+          alpha = ex2(m_used - mb);
+          m_used = mb;
+        }
+        if (__any_sync(0xffffffffu, redo)) {
+          // rare: some row's maximum passed its base by more than the threshold; the warp
+          // redoes the block (rows that keep their base recompute the same P)
+          l = l * alpha + p_from_sv(m_used);
+          rescale_o(alpha);
+        } else {
+          const uint64_t accs = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
+          l += lo_f32(accs) + hi_f32(accs);
+        }
+      } else {
+        // a row's first block, or a block with masked keys: the block maximum first
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld_x32(s_addr + c * 32, sv[c]);
+        ptx::tmem_ld_wait();
+        // four independent max chains (one per 32-column chunk) keep the dependency short
+        float mc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (lim >= kBk - 1) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              mc[c] = max3(mc[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float x = c * 32 + e <= lim ? __uint_as_float(sv[c][e]) : -INFINITY;
+              sv[c][e] = __float_as_uint(x);
+              mc[c] = fmaxf(mc[c], x);
+            }
+        }
+        const float mb = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c1;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mb > m_used + kRescaleThreshold) {
+          if (m_used != -INFINITY) {
+            alpha = ex2(m_used - mb);
+            rescale = true;
+            l *= alpha;
+          }
+          m_used = mb;
+        }
+        l += p_from_sv(m_used == -INFINITY ? 0.f : m_used);
+        if (__any_sync(0xffffffffu, rescale)) rescale_o(alpha);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();

@@ -184,3 +184,26 @@ def make_paged_decode_inputs(cfg: MsaConfig, seq_lens, device="cpu", seed: int |
         "block_table": torch.from_numpy(table).to(dev),
         "n_phys": P,
     }
+
+
+def add_score_ramp(x: dict, per_key: float, seed: int = 0) -> dict:
+    """Prefill inputs whose attention logits climb along the sequence for half of the query
+    heads: a unit vector u (numpy ``default_rng(seed)``) gets weight ``per_key * j / 10`` in
+    key j of every KV head and weight 10 in every even query head, so q.k grows by
+    ``per_key`` per key for even heads and not at all for odd ones.  Each later block then
+    raises an even head's running row maximum by a wide margin while the odd heads' maxima
+    stay put (the softmax's rescaling path, taken by some rows of a tile and not others).
+    Returns new q and k tensors (same dtype and device); v and the index tensors are kept."""
+    q, k = x["q"], x["k"]
+    d = q.shape[-1]
+    u = np.random.default_rng(seed).standard_normal(d)
+    u = torch.from_numpy(u / np.linalg.norm(u)).float()
+    T = k.shape[2]
+    ramp = (per_key / 10.0) * torch.arange(T, dtype=torch.float32)[:, None] * u[None, :]
+    k2 = (k.float().cpu() + ramp[None, None]).to(k.dtype).to(k.device)
+    even = torch.zeros(q.shape[2], 1)
+    even[0::2] = 10.0
+    q2 = (q.float().cpu() + even[None, None] * u[None, None, None]).to(q.dtype).to(q.device)
+    out = dict(x)
+    out["q"], out["k"] = q2, k2
+    return out

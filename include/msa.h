@@ -133,11 +133,17 @@ msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void*
  * dk and dv [batch, n_heads_kv, seq_k, head_dim] (cleared on the stream, then accumulated:
  * a key block selected by several tiles collects all their contributions).  With p the
  * attention weights, D = dout . out, ds = p (dout . v - D): dq = sm_scale sum ds k,
- * dk += sm_scale ds q, dv += p dout.  CUDA cores, fp32. */
+ * dk += sm_scale ds q, dv += p dout.  bf16 shapes with head_dim 128, block 128, q_tile 64
+ * run on the tensor cores (a query-tile pass for dq, a key-block pass for dk / dv) and need
+ * a device workspace of msa_workspace_bytes(shape, 2) bytes (per-row D and a bitmap of
+ * which tiles selected which blocks); other shapes run on CUDA cores and need none
+ * (workspace may then be null).  dk / dv sums over several CTAs use fp32 atomics, so their
+ * last bits can vary from run to run. */
 msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, const void* k,
                                        const void* v, const int32_t* sel, const void* out,
                                        const float* lse, const void* dout, float* dq, float* dk,
-                                       float* dv, void* stream);
+                                       float* dv, void* workspace, size_t ws_bytes,
+                                       void* stream);
 
 /* Training the index branch (the pages: the index branch is trained with a KL loss to match
  * the main branch's attention).  The pages give no formula; this library's reading: for
@@ -214,8 +220,9 @@ msa_status msa_sparse_decode_paged(const msa_shape* shape, const int32_t* seq_le
                                    void* out, float* lse, void* workspace, size_t ws_bytes,
                                    void* stream);
 
-/* Scratch bytes msa_sparse_prefill (which = 0) or msa_sparse_decode (which = 1) needs for
- * this shape; 0 when none.  Returns 0 for an invalid shape. */
+/* Scratch bytes msa_sparse_prefill (which = 0), msa_sparse_decode (which = 1) or
+ * msa_sparse_prefill_backward (which = 2) needs for this shape; 0 when none.  Returns 0
+ * for an invalid shape. */
 size_t msa_workspace_bytes(const msa_shape* shape, int which);
 
 /* Synchronises `stream`, then reports (and clears) the device status word and any pending

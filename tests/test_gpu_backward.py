@@ -18,6 +18,11 @@ CASES = {
     "bf16_d64_g16": CONFIGS["p32k"].with_(seq=2048, head_dim=64, n_heads_q=64, top_k=6),
     "bf16_4096_k16": CONFIGS["p32k"].with_(seq=4096, n_plants=0),
     "bf16_qt128_ragged": CONFIGS["p32k"].with_(seq=1500, q_tile=128, top_k=4, n_plants=0),
+    # tensor-core path: G = 16, 4, 2; k = 1; and blocks selected by tiles of several dK/dV CTAs
+    "bf16_g16_3000": CONFIGS["p32k"].with_(seq=3000, n_heads_q=64, top_k=8, n_plants=0),
+    "bf16_g4_k1": CONFIGS["p32k"].with_(seq=1200, n_heads_q=16, top_k=1, n_plants=0),
+    "bf16_g2_ragged": CONFIGS["p32k"].with_(seq=700, n_heads_q=8, top_k=3, n_plants=0),
+    "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=0),
 }
 
 
@@ -38,8 +43,10 @@ def test_sparse_prefill_backward(name):
     dq = torch.full(x["q"].shape, float("nan"), device="cuda")
     dk = torch.full(x["k"].shape, float("nan"), device="cuda")
     dv = torch.full(x["v"].shape, float("nan"), device="cuda")
+    ws_bytes = _lib.msa_workspace_bytes(shape, 2)
+    ws = torch.full((ws_bytes // 4 + 1,), float("nan"), device="cuda") if ws_bytes else None
     _lib.msa_sparse_prefill_backward(shape, x["q"], x["k"], x["v"], sel, out, lse, dout,
-                                     dq, dk, dv)
+                                     dq, dk, dv, ws)
     _lib.msa_get_device_status()
     rq, rk, rv = oracle.sparse_attention_backward(x["q"], x["k"], x["v"], sel_np, dout,
                                                   cfg.block_size, cfg.q_tile)

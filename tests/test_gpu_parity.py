@@ -14,8 +14,8 @@ from block_sparse_gqa_02_gb300 import _lib
 from block_sparse_gqa_02_gb300.api import (alloc_decode_outputs, alloc_prefill_outputs,
                                            run_decode, run_prefill)
 from block_sparse_gqa_02_gb300.configs import CONFIGS
-from block_sparse_gqa_02_gb300.inputs import (make_inputs, random_block_scores,
-                                              random_selection)
+from block_sparse_gqa_02_gb300.inputs import (add_score_ramp, make_inputs,
+                                              random_block_scores, random_selection)
 from tests.parity import (check_lse, check_out, check_scores, check_selection_valid,
                           sample_tiles, to_np)
 
@@ -222,6 +222,34 @@ def test_sparse_attention(name):
     got_o, got_l, ref_o, ref_l = _attn_case(cfg)
     check_out(got_o, ref_o, cfg.dtype, name)
     check_lse(got_l, ref_l, cfg.dtype, name)
+
+
+@pytest.mark.parametrize("per_key", [0.75, 3.0])
+def test_prefill_rows_rescale_unevenly(per_key):
+    """Even heads' row maxima climb by ~94 (0.75 per key) or ~380 logits per block, far past
+    the softmax's rescale threshold, while odd heads' stay flat: rows of one warp take the
+    rescaling path and rows beside them do not."""
+    cfg = small_cfg("p32k", seq=2000, top_k=6, n_plants=0)
+    x = add_score_ramp(make_inputs(cfg, device=DEV), per_key, seed=3)
+    shape = _lib.shape_from_config(cfg)
+    ncand = cur_blocks(shape) + 1
+    sel_np = random_selection(np.broadcast_to(ncand, (1, 4, len(ncand))), cfg.top_k, 4)
+    sel = torch.from_numpy(sel_np).to(DEV)
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((1, cfg.n_heads_q, cfg.seq), dtype=torch.float32, device=DEV)
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    _lib.msa_get_device_status()
+    ref_o, ref_l = oracle.sparse_attention(x["q"], x["k"], x["v"], sel_np, cfg.block_size,
+                                           cfg.q_tile)
+    check_out(out, ref_o, "bf16", f"ramp {per_key}")
+    # lse grows with the logits (to ~130 and ~520 here): the fp32 accumulation of Q.K^T
+    # adds an error proportional to it
+    lse_ref = np.asarray(ref_l)
+    tol = 2e-3 + 1e-4 * np.abs(lse_ref)
+    got = to_np(lse)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(fin, np.isfinite(got))
+    assert np.all(np.abs(got[fin] - lse_ref[fin]) <= tol[fin])
 
 
 def test_sparse_prefill_p32k_sampled():

@@ -56,7 +56,7 @@ def test_static_scratch_decode_matches_regular_twice():
 def test_static_scratch_rejects_oversized_shapes():
     """A shape whose scratch exceeds the static array is refused before anything runs."""
     lib = _lib.load()
-    shape = _lib.make_shape(1, 1, 1 << 16, 512, 8, 128, 128, 128, 64, 1, "bf16")
+    shape = _lib.make_shape(64, 1, 1 << 16, 512, 8, 128, 128, 128, 64, 1, "bf16")
     need = lib.msa_workspace_bytes(ctypes.byref(shape), 1)
     assert need > (8 << 20)
     fake = 1 << 20
