@@ -68,11 +68,18 @@ def decode_bytes(cfg):
 # that was profiled: a changed kernel reports null until it is captured again.
 MEASURED_TRAFFIC = {
     "sparse_prefill_tc.cu": {
-        "sha256_16": "6983e3bc97910a68",
+        "sha256_16": "95e1cb0cc5ae2281",
         "workload": "p128k",
         "bytes_per_launch": 4.53e9,
         "how": "dram__bytes_read.sum + dram__bytes_write.sum of one p32k launch "
-               "(336.2 + 229.5 MB), scaled by the (token, query head) rows to 128K (x8)",
+               "(336.4 + 230.0 MB), scaled by the (token, query head) rows to 128K (x8)",
+    },
+    "index_scan_tc.cu": {
+        "sha256_16": "f9e04bc1efc0b433",
+        "workload": "d1m",
+        "bytes_per_launch": 2.18e9,
+        "how": "dram__bytes_read.sum + dram__bytes_write.sum of one launch with 131072-token "
+               "caches (268.5 + 4.1 MB), scaled by the cache length to 1M (x8)",
     },
 }
 
@@ -484,7 +491,9 @@ def run_ours(args, rank, world, device):
                            "sparse_decode+combine": d_attn * 1e3},
             "roofline": {"bound": "hbm", "kernel": "decode index scan", "achieved": scan_gbs,
                          "peak": hbm_peak, "unit": "GB/s", "frac": scan_gbs / hbm_peak,
-                         "traffic": None, "algorithmic_bytes_per_launch": b_scan},
+                         "traffic": measured_traffic("index_scan_tc.cu", dcfg.name),
+                         "traffic_note": MEASURED_TRAFFIC["index_scan_tc.cu"]["how"],
+                         "algorithmic_bytes_per_launch": b_scan},
             "step_hbm_gbs": (b_scan + b_rest) / (d_total / 1e3) / 1e9,
             "dense_bytes_avoided": b_dense - (b_scan + b_rest),
         }
