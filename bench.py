@@ -230,6 +230,23 @@ class Step:
         return np.array(out)
 
 
+def gpu_local_cpus(device):
+    """CPUs the GPU's PCI device reports as local (sysfs), within this process's allowed
+    set; empty when unknown."""
+    try:
+        prop = torch.cuda.get_device_properties(device)
+        path = (f"/sys/bus/pci/devices/{prop.pci_domain_id:04x}:{prop.pci_bus_id:02x}:"
+                f"{prop.pci_device_id:02x}.0/local_cpulist")
+        cpus = set()
+        with open(path) as f:
+            for part in f.read().strip().split(","):
+                lo, _, hi = part.partition("-")
+                cpus.update(range(int(lo), int(hi or lo) + 1))
+        return cpus & os.sched_getaffinity(0)
+    except (OSError, ValueError, AttributeError):
+        return set()
+
+
 def e2e_prefill(cfg, step, stream, n_steps):
     """The same metric through the public API with host buffers.  Every step copies its own
     inputs (q, k, v, idx_q, idx_k) from pinned host memory to the device, runs the three
@@ -240,11 +257,22 @@ def e2e_prefill(cfg, step, stream, n_steps):
     reported alongside."""
     names = ["q", "k", "v", "idx_q", "idx_k"]
     dev0 = step.x["q"].device
-    host = {n: step.x[n].cpu().pin_memory() for n in names}
-    out_h = [torch.empty(step.bufs["out"].shape, dtype=step.bufs["out"].dtype).pin_memory()
-             for _ in range(2)]
-    lse_h = [torch.empty(step.bufs["lse"].shape, dtype=torch.float32).pin_memory()
-             for _ in range(2)]
+    # pinned host buffers on the memory next to this GPU: allocate them from the CPUs its
+    # PCI device reports as local (a far NUMA node halves the copy bandwidth)
+    local = gpu_local_cpus(dev0)
+    saved = os.sched_getaffinity(0)
+    if local:
+        os.sched_setaffinity(0, local)
+    try:
+        host = {n: step.x[n].cpu().pin_memory() for n in names}
+        out_h = [torch.empty(step.bufs["out"].shape, dtype=step.bufs["out"].dtype).pin_memory()
+                 for _ in range(2)]
+        lse_h = [torch.empty(step.bufs["lse"].shape, dtype=torch.float32).pin_memory()
+                 for _ in range(2)]
+    finally:
+        os.sched_setaffinity(0, saved)
+    host_note = (f"pinned buffers allocated from the {len(local)} GPU-local CPUs"
+                 if local else "GPU-local CPU list unavailable; default placement")
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h[0].numel() * out_h[0].element_size() + lse_h[0].numel() * 4
     dev = [{n: torch.empty_like(step.x[n]) for n in names} for _ in range(2)]
@@ -292,7 +320,7 @@ def e2e_prefill(cfg, step, stream, n_steps):
             "ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n_steps, "pipelined": "copy-in / compute / copy-out on three streams",
             "serial_value": cfg.seq * cfg.batch / (ms_serial / 1e3),
-            "serial_ms_per_step": ms_serial}, host
+            "serial_ms_per_step": ms_serial, "host_memory": host_note}, host
 
 
 def prefill_1m(args, device, stream, flush, tc_peak):
@@ -364,12 +392,41 @@ def backward_32k(args, device, stream, flush, tc_peak):
     ms = float(np.median(ts))
     _, f_sparse, _ = prefill_flops(cfg)
     f_bwd = f_sparse * 2.5          # Q.K^T, dout.V^T, dQ, dK, dV: 10 d per (row, key)
+
+    # the index branch's KL loss and its gradients on the same selection
+    loss = torch.empty(1, device=device)
+    diq = torch.empty(x["idx_q"].shape, device=device)
+    dik = torch.empty(x["idx_k"].shape, device=device)
+
+    def run_kl():
+        _lib.msa_index_kl_loss(step.shape, x["q"], x["k"], b["lse"], x["idx_q"], x["idx_k"],
+                               b["sel"], loss, diq, dik, stream)
+    run_kl()
+    kl_ts = []
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+        e0.record(stream)
+        run_kl()
+        e1.record(stream)
+        stream.synchronize()
+        kl_ts.append(e0.elapsed_time(e1))
+    _lib.msa_get_device_status(stream)
+    kl_ms = float(np.median(kl_ts))
+    # per (token, KV head, visible selected key): the G heads' logits for the target
+    # (2 d G) and the index logit, d idx_q and d idx_k (3 x 2 dI)
+    G, d, dI = cfg.n_heads_q // cfg.n_heads_kv, cfg.head_dim, cfg.index_dim
+    f_kl = f_sparse / (4 * d * G) * (2 * d * G + 6 * dI)
     del step
     torch.cuda.empty_cache()
     return {"workload": f"{cfg.name}: {cfg.description}", "ms": ms,
             "algorithmic_flops": f_bwd, "tflops": f_bwd / (ms / 1e3) / 1e12,
             "frac_of_tensor_peak": f_bwd / (ms / 1e3) / 1e12 / tc_peak,
-            "kernel": "tcgen05: dQ pass over query tiles, dK/dV pass over key blocks"}
+            "kernel": "tcgen05: dQ pass over query tiles, dK/dV pass over key blocks",
+            "index_kl": {"ms": kl_ms, "algorithmic_flops": f_kl,
+                         "tflops": f_kl / (kl_ms / 1e3) / 1e12,
+                         "kernel": "CUDA cores, fp32 (loss, d idx_q, d idx_k)"}}
 
 
 def cpu_baseline_prefill(cfg, host, budget_s=15.0, seed=0):
