@@ -398,9 +398,12 @@ def backward_32k(args, device, stream, flush, tc_peak):
     diq = torch.empty(x["idx_q"].shape, device=device)
     dik = torch.empty(x["idx_k"].shape, device=device)
 
+    kl_ws_bytes = _lib.msa_workspace_bytes(step.shape, 3)
+    kl_ws = torch.empty(kl_ws_bytes // 4 + 1, device=device) if kl_ws_bytes else None
+
     def run_kl():
         _lib.msa_index_kl_loss(step.shape, x["q"], x["k"], b["lse"], x["idx_q"], x["idx_k"],
-                               b["sel"], loss, diq, dik, stream)
+                               b["sel"], loss, diq, dik, kl_ws, stream=stream)
     run_kl()
     kl_ts = []
     for _ in range(3):
@@ -426,7 +429,8 @@ def backward_32k(args, device, stream, flush, tc_peak):
             "kernel": "tcgen05: dQ pass over query tiles, dK/dV pass over key blocks",
             "index_kl": {"ms": kl_ms, "algorithmic_flops": f_kl,
                          "tflops": f_kl / (kl_ms / 1e3) / 1e12,
-                         "kernel": "CUDA cores, fp32 (loss, d idx_q, d idx_k)"}}
+                         "kernel": "tcgen05: query-tile pass (loss, d idx_q), key-block pass "
+                                   "(d idx_k)"}}
 
 
 def cpu_baseline_prefill(cfg, host, budget_s=15.0, seed=0):

@@ -47,7 +47,8 @@ SIGNATURES = {
     "msa_sparse_decode": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "msa_sparse_prefill_backward": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                            _vp, _vp, _vp, _sz, _vp]),
-    "msa_index_kl_loss": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "msa_index_kl_loss": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                 _sz, _vp]),
     "msa_sparse_decode_static": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "msa_index_scores_paged": (_i32, [_SHAPE_P, _vp, _vp, _i32, _vp, _vp, _vp, _vp]),
     "msa_block_topk_ragged": (_i32, [_SHAPE_P, _vp, _vp, _vp, _vp]),
@@ -181,10 +182,13 @@ def msa_sparse_prefill_backward(shape: MsaShape, q, k, v, sel, out, lse, dout, d
 
 
 def msa_index_kl_loss(shape: MsaShape, q, k, lse, idx_q, idx_k, sel, loss, d_idx_q, d_idx_k,
-                      stream=None):
+                      workspace=None, ws_bytes=None, stream=None):
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().msa_index_kl_loss(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(lse),
                                     _ptr(idx_q), _ptr(idx_k), _ptr(sel), _ptr(loss),
-                                    _ptr(d_idx_q), _ptr(d_idx_k), _stream(stream)),
+                                    _ptr(d_idx_q), _ptr(d_idx_k), _ptr(workspace), ws_bytes,
+                                    _stream(stream)),
            "msa_index_kl_loss")
 
 

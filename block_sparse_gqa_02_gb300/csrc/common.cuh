@@ -99,7 +99,10 @@ size_t backward_workspace_bytes(const Dims& p);
 // cleared then accumulated; fp32.
 cudaError_t launch_index_kl(const Dims& p, const void* q, const void* k, const float* lse,
                             const void* idx_q, const void* idx_k, const int32_t* sel,
-                            float* loss, float* d_idx_q, float* d_idx_k, cudaStream_t st);
+                            float* loss, float* d_idx_q, float* d_idx_k, void* workspace,
+                            cudaStream_t st, int* status);
+// Workspace bytes of the index KL (0 on the CUDA-core path).
+size_t index_kl_workspace_bytes(const Dims& p);
 
 // Decode split-KV: number of block groups each (sequence, KV head) is split into, and
 // the scratch it needs (partial outputs and partial log-sum-exps, fp32).

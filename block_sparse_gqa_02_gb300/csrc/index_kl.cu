@@ -15,6 +15,7 @@
 // d idx_k over the CTA's tokens in shared memory before fp32 atomics (index keys are shared
 // by every tile and head).  CUDA cores, fp32.
 #include "common.cuh"
+#include "index_kl_tc.cuh"
 
 namespace msa {
 
@@ -242,9 +243,17 @@ cudaError_t kl(const Dims& p, const void* q, const void* k, const float* lse, co
 
 }  // namespace
 
+size_t index_kl_workspace_bytes(const Dims& p) {
+  return index_kl_tc_supported(p) ? index_kl_tc_workspace_bytes(p) : 0;
+}
+
 cudaError_t launch_index_kl(const Dims& p, const void* q, const void* k, const float* lse,
                             const void* idx_q, const void* idx_k, const int32_t* sel,
-                            float* loss, float* d_idx_q, float* d_idx_k, cudaStream_t st) {
+                            float* loss, float* d_idx_q, float* d_idx_k, void* workspace,
+                            cudaStream_t st, int* status) {
+  if (index_kl_tc_supported(p))
+    return launch_index_kl_tc(p, q, k, lse, idx_q, idx_k, sel, loss, d_idx_q, d_idx_k, workspace,
+                              st, status);
   if (p.dtype == 1) {
     if (p.d == 128)
       return p.dI == 128 ? kl<__nv_bfloat16, 128, 128>(p, q, k, lse, idx_q, idx_k, sel, loss,

@@ -1,0 +1,723 @@
+// Training the index branch on the tcgen05 tensor cores: the KL loss toward the main
+// branch's attention and its gradients ("Sparse Attention Cannot Be Directly Ported Across
+// Architectures", paragraph introducing MSA; aietalks.com, "MSA uses a lightweight index
+// branch before sparse attention": the index branch is trained with a KL loss to match the
+// main branch's attention).  bf16 inputs, head_dim = index_dim = 128, 128-key blocks,
+// 64-query tiles, G = 2 .. 32 query heads per KV head; fp32 accumulation and outputs.
+//
+// For token t and KV head g over the keys J of the tile's selected blocks (j <= t):
+//   target p_T[j] = mean over the group's G heads h of 2^(c1 s_hj - lse2_h)   (held constant)
+//   index  p_I[j] = 2^(c2 z_j - lseI2),  z_j = idx_q[t,g] . idx_k[j],  c2 = index_scale log2 e
+//   loss += sum_j p_T (ln p_T - ln p_I);  gz_j = p_I - p_T = dloss / d(index_scale z_j)
+//   d idx_q[t,g] = index_scale sum_j gz_j idx_k[j];  d idx_k[j] += index_scale gz_j idx_q[t,g].
+//
+// Two kernels:
+// * rows (query-tile order, one CTA per 128 (token, head) rows like the forward): a first
+//   pass over the blocks forms lseI2 from Z = idx_q idx_k^T, with each row's idx_q replicated
+//   so that every row of a token holds its token's index logits; a second pass forms S and Z
+//   again, the math warps average the G rows of a token with warp shuffles, accumulate the
+//   loss and write gz into TMEM, and d idx_q += gz idx_k accumulates in TMEM.
+// * keys (key-block order over the tiles that selected the block, as in the dK/dV pass of
+//   the backward): S^T = K Q^T and Z^T = idx_k idx_q^T with the keys on the TMEM lanes, so a
+//   token's G rows are adjacent columns; gz^T goes to TMEM and d idx_k += gz^T idx_q
+//   accumulates there over all of the CTA's groups before one set of vector atomics.
+// Every wait is bounded.
+#include "common.cuh"
+#include "index_kl_tc.cuh"
+#include "ptx.cuh"
+#include "sparse_backward_tc.cuh"
+#include "tma_host.cuh"
+
+namespace msa {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBk = 128;
+constexpr int kQt = 64;
+constexpr int kRows = 128;
+constexpr int kRowBytes = 128;
+constexpr int kTileBytes = 2 * kRows * kRowBytes;           // [2 chunks][128 rows][128 B]
+constexpr int kMaxSel = 256;
+constexpr int kThreads = 192;                               // 4 math warps, producer, MMA
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);
+constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kMaxTilesPerCta = 2048;
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// D[tmem] = A[smem, K-major, 128 rows] B[smem, K-major]^T over 128 (8 steps of 16); the B
+// tile's two 64-element chunks lie b_chunk bytes apart.
+__device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                       uint32_t b_chunk, uint32_t idesc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t in = (kk & 3) * 32;
+    ptx::umma_bf16_ss(d_tmem, ptx::smem_desc_k_sw128(a_smem + (kk >> 2) * (kRows * kRowBytes) + in),
+                      ptx::smem_desc_k_sw128(b_smem + (kk >> 2) * b_chunk + in), idesc,
+                      kk > 0 ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void raise_abort(int* abort_flag, int* status, int code) {
+  *abort_flag = 1;
+  if (status) atomicExch(status, code);
+}
+
+// ===================================================================== rows kernel
+
+struct __align__(1024) SmemR {
+  uint8_t q[kTileBytes];        // Q rows of the group
+  uint8_t iqr[kTileBytes];      // row R: idx_q of R's token (K-major, 128-byte swizzle)
+  uint8_t k[2][kTileBytes];
+  uint8_t ik[2][kTileBytes];
+  uint64_t q_full, ring_full[2], ring_empty[2];
+  uint64_t z_full[2], z_free[2], pass1_done;
+  uint64_t s_full, g_full, dq_done, drain;
+  int blocks[kMaxSel];
+  int n_sel;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_ik,
+                  const __nv_bfloat16* __restrict__ idx_q, const int32_t* __restrict__ sel,
+                  const float* __restrict__ lse, float* __restrict__ lse_i, float* __restrict__ loss,
+                  float* __restrict__ d_idx_q, Dims p, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemR& s = *reinterpret_cast<SmemR*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  constexpr int kTokPerGroup = kRows / G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int part = blockIdx.x;
+  const int m = p.nR - 1 - blockIdx.y;
+  const int bg = blockIdx.z, b = bg / p.Hkv, g = bg % p.Hkv;
+  const int t0 = m * kQt + part * kTokPerGroup;
+  const volatile int* abort = &s.abort;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&s.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.ring_full[i], 1);
+      ptx::mbar_init(&s.ring_empty[i], 1);
+      ptx::mbar_init(&s.z_full[i], 1);
+      ptx::mbar_init(&s.z_free[i], 4);
+    }
+    ptx::mbar_init(&s.pass1_done, 4);
+    ptx::mbar_init(&s.s_full, 1);
+    ptx::mbar_init(&s.g_full, 4);
+    ptx::mbar_init(&s.dq_done, 1);
+    ptx::mbar_init(&s.drain, 1);
+    s.abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&s.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 1) {
+    const int32_t* srow = sel + ((size_t)bg * p.nR + m) * p.k;
+    int n = 0;
+    for (int i0 = 0; i0 < p.k; i0 += 32) {
+      const int i = i0 + lane;
+      const int blk = i < p.k ? srow[i] : -1;
+      const bool ok = blk >= 0 && blk < p.nB;
+      const unsigned mask = __ballot_sync(0xffffffffu, ok);
+      if (ok) s.blocks[n + __popc(mask & ((1u << lane) - 1))] = blk;
+      n += __popc(mask);
+    }
+    if (lane == 0) s.n_sel = n;
+  }
+  if (warp < 4) {
+    // row r's copy of its token's index query, written in the 128-byte-swizzled K-major
+    // layout the tensor core reads (16-byte unit u of row r at unit u ^ (r % 8))
+    const int r = warp * 32 + lane;
+    const int t = t0 + r / G;
+    const uint4* src = reinterpret_cast<const uint4*>(idx_q + (((size_t)b * p.Sq + (t < p.Sq ? t : 0)) * p.Hkv + g) * kD);
+#pragma unroll
+    for (int u16 = 0; u16 < 16; ++u16) {
+      const uint4 v = t < p.Sq ? src[u16] : make_uint4(0, 0, 0, 0);
+      const int kc = u16 >> 3, u = u16 & 7;
+      *reinterpret_cast<uint4*>(s.iqr + kc * (kRows * kRowBytes) + r * kRowBytes +
+                                ((u ^ (r & 7)) << 4)) = v;
+    }
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+  const int n_sel = s.n_sel;
+  // TMEM: pass 1 Z in [0,128) / [128,256) alternately; pass 2 S [0,128) (gz bf16 over its
+  // first 64), Z [128,256), dIQ [256,384)
+  constexpr uint32_t kColS = 0, kColZ = 128, kColDQ = 256;
+
+  if (warp == kProducerWarp) {
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0 && n_sel > 0) {
+      ptx::mbar_arrive_expect_tx(&s.q_full, kTileBytes);
+      for (int kc = 0; kc < 2; ++kc)
+        ptx::tma_load_4d(s.q + kc * kRows * kRowBytes, &tm_q, &s.q_full, kc * 64, g * G, t0, b);
+    }
+    // the block ring: pass 1 loads idx_k blocks, pass 2 idx_k and K blocks
+    for (int rr = 0; rr < 2 * n_sel; ++rr) {
+      const int st = rr & 1;
+      if (!ptx::mbar_wait(&s.ring_empty[st], ((rr >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+      if (lane == 0) {
+        const bool pass2 = rr >= n_sel;
+        const int blk = s.blocks[pass2 ? rr - n_sel : rr];
+        ptx::mbar_arrive_expect_tx(&s.ring_full[st], pass2 ? 2 * kTileBytes : kTileBytes);
+        for (int kc = 0; kc < 2; ++kc) {
+          ptx::tma_load_3d(s.ik[st] + kc * kBk * kRowBytes, &tm_ik, &s.ring_full[st], kc * 64,
+                           blk * kBk, b);
+          if (pass2)
+            ptx::tma_load_3d(s.k[st] + kc * kBk * kRowBytes, &tm_k, &s.ring_full[st], kc * 64,
+                             blk * kBk, bg);
+        }
+      }
+      issued = rr + 1;
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x701);
+    if (*abort && lane == 0 && n_sel > 0) {
+      ptx::mbar_wait_timed(&s.q_full, 0);
+      for (int rr = issued > 2 ? issued - 2 : 0; rr < issued; ++rr)
+        ptx::mbar_wait_timed(&s.ring_full[rr & 1], (rr >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    bool ok = true, issued_any = false;
+    const uint32_t qa = ptx::smem_u32(s.q), za = ptx::smem_u32(s.iqr);
+    for (int j = 0; ok && j < n_sel; ++j) {                  // pass 1
+      const int st = j & 1, buf = j & 1;
+      if (!ptx::mbar_wait(&s.ring_full[st], (j >> 1) & 1, abort) ||
+          !ptx::mbar_wait(&s.z_free[buf], ((j >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if (lane == 0) {
+        mma_kk(tmem + buf * 128, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
+        ptx::umma_commit(&s.z_full[buf]);
+        ptx::umma_commit(&s.ring_empty[st]);
+      }
+      issued_any = true;
+      __syncwarp();
+    }
+    if (ok && n_sel > 0)
+      ok = ptx::mbar_wait(&s.pass1_done, 0, abort) && ptx::mbar_wait(&s.q_full, 0, abort);
+    for (int j = 0; ok && j < n_sel; ++j) {                  // pass 2
+      const int rr = n_sel + j, st = rr & 1;
+      if (!ptx::mbar_wait(&s.ring_full[st], (rr >> 1) & 1, abort) ||
+          (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort))) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if (lane == 0) {
+        mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[st]), kBk * kRowBytes, kIdescKK);
+        mma_kk(tmem + kColZ, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
+        ptx::umma_commit(&s.s_full);
+      }
+      __syncwarp();
+      if (!ptx::mbar_wait(&s.g_full, j & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if (lane == 0) {
+        // dIQ += gz idx_k: gz (rows x keys) from TMEM, idx_k as the MN-major B operand
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::umma_bf16_ts(tmem + kColDQ, tmem + kColS + kk * 8,
+                            ptx::smem_desc_mn_sw128(ptx::smem_u32(s.ik[st]) + kk * 16 * kRowBytes,
+                                                    kBk * kRowBytes, 1024),
+                            kIdescMN, (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::umma_commit(&s.dq_done);
+        ptx::umma_commit(&s.ring_empty[st]);
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x702);
+    if (*abort && lane == 0 && issued_any) {
+      ptx::umma_commit(&s.drain);
+      ptx::mbar_wait_timed(&s.drain, 0);
+    }
+  } else {
+    // ------------------------------------------------ math warps 0-3: one row each
+    const int r = warp * 32 + lane;
+    const int t = t0 + r / G, hh = r % G, h = g * G + hh;
+    const bool valid = t < p.Sq;
+    const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    bool ok = true;
+    // pass 1: log2-sum-exp of the index logits over the tile's visible keys
+    float mI = -INFINITY, lI = 0.f;
+    for (int j = 0; j < n_sel; ++j) {
+      const int buf = j & 1, lim = t - s.blocks[j] * kBk;
+      if (!ptx::mbar_wait(&s.z_full[buf], (j >> 1) & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t zv[32];
+        ptx::tmem_ld_x32(tmem + lane_off + buf * 128 + c * 32, zv);
+        ptx::tmem_ld_wait();
+        float cm = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          if (c * 32 + e <= lim) cm = fmaxf(cm, __uint_as_float(zv[e]) * c2);
+        if (cm != -INFINITY) {
+          const float mn = fmaxf(mI, cm);
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (c * 32 + e <= lim) acc += ex2(fmaf(__uint_as_float(zv[e]), c2, -mn));
+          lI = lI * ex2(mI - mn) + acc;
+          mI = mn;
+        }
+      }
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.z_free[buf]);
+    }
+    const float lseI2 = mI == -INFINITY ? -INFINITY : mI + __log2f(lI);
+    if (ok && valid && hh == 0) lse_i[((size_t)b * p.Hkv + g) * p.Sq + t] = lseI2;
+    ptx::tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&s.pass1_done);
+    // pass 2: target, loss, gz
+    const float lse2 = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
+    float lsum = 0.f;
+    for (int j = 0; ok && j < n_sel; ++j) {
+      const int lim = t - s.blocks[j] * kBk;
+      if (!ptx::mbar_wait(&s.s_full, j & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], zv[32];
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
+        ptx::tmem_ld_x32(tmem + lane_off + kColZ + c * 32, zv);
+        ptx::tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float gz2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const bool vis = c * 32 + e + u <= lim;
+            float pt = vis ? ex2(fmaf(__uint_as_float(sv[e + u]), c1, -lse2)) : 0.f;
+#pragma unroll
+            for (int o = 1; o < G; o <<= 1) pt += __shfl_xor_sync(0xffffffffu, pt, o);
+            pt *= 1.f / G;
+            const float zl = fmaf(__uint_as_float(zv[e + u]), c2, -lseI2);   // log2 p_I
+            const float pi = vis ? ex2(zl) : 0.f;
+            if (hh == 0 && pt > 0.f) lsum += pt * (__log2f(pt) - zl);
+            gz2[u] = pi - pt;
+          }
+          pk[e >> 1] = pack_bf16x2(gz2[0], gz2[1]);
+        }
+        // gz chunk c over S columns 16c .. 16c+15 (already loaded)
+        ptx::tmem_st_x16(tmem + lane_off + kColS + c * 16, pk);
+      }
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.g_full);
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x703);
+    const bool have = ok && n_sel > 0 && ptx::mbar_wait(&s.dq_done, (n_sel - 1) & 1, abort);
+    if (have) ptx::tc_fence_after_sync();
+    float* dst = d_idx_q + (((size_t)b * p.Sq + (valid ? t : 0)) * p.Hkv + g) * kD;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      if (have) {
+        ptx::tmem_ld_x32(tmem + lane_off + kColDQ + c * 32, v);
+        ptx::tmem_ld_wait();
+      }
+      if (valid && hh == 0) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + c * 32 + e) =
+              have ? make_float4(__uint_as_float(v[e]) * p.index_scale,
+                                 __uint_as_float(v[e + 1]) * p.index_scale,
+                                 __uint_as_float(v[e + 2]) * p.index_scale,
+                                 __uint_as_float(v[e + 3]) * p.index_scale)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    // the loss of this warp's rows (one lane per token), natural log
+    float lv = lsum * kLn2;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
+    if (lane == 0 && lv != 0.f) atomicAdd(loss, lv);
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ===================================================================== keys kernel
+
+constexpr int kIqRows = 64;                                   // idx_q rows of a group, padded
+constexpr int kIqBytes = 2 * kIqRows * kRowBytes;             // [2 chunks][64 rows][128 B]
+
+struct __align__(1024) SmemK {
+  uint8_t k[kTileBytes];
+  uint8_t ik[kTileBytes];
+  uint8_t q[2][kTileBytes];
+  uint8_t iq[2][kIqBytes];
+  float lse2[2][kRows];
+  float lseI2[2][kIqRows];
+  uint64_t kv_full, g_full[2], g_empty[2];
+  uint64_t s_full, p_full, acc_done, drain;
+  int tiles[kMaxTilesPerCta];
+  int n_tiles;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_ik, const __grid_constant__ CUtensorMap tm_iq,
+                  const uint32_t* __restrict__ bits, const float* __restrict__ lse,
+                  const float* __restrict__ lse_i, float* __restrict__ d_idx_k, Dims p, int words,
+                  int words_per_cta, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemK& s = *reinterpret_cast<SmemK*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  constexpr int kTok = kRows / G;                             // tokens of a 128-row group
+  constexpr int kNTok = kTok < 16 ? 16 : kTok;                // UMMA N (and K of d idx_k)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = blockIdx.x, blk = blockIdx.y, bg = blockIdx.z;
+  const int b = bg / p.Hkv, g = bg % p.Hkv;
+  const int parts = p.Qt * G / kRows;
+
+  if (warp == 0) {
+    const uint32_t* row = bits + ((size_t)bg * p.nB + blk) * words;
+    const int w0 = chunk * words_per_cta, w1 = min(words, w0 + words_per_cta);
+    int n = 0;
+    for (int wb = w0; wb < w1; wb += 32) {
+      const int w = wb + lane;
+      const uint32_t word = w < w1 ? row[w] : 0u;
+      const int cnt = __popc(word);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int pos = n + incl - cnt;
+      for (uint32_t x = word; x; x &= x - 1) s.tiles[pos++] = w * 32 + __ffs(x) - 1;
+      n += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) s.n_tiles = n;
+  }
+  __syncthreads();
+  const int n_tiles = s.n_tiles;
+  if (n_tiles == 0) return;                                   // the whole CTA leaves together
+  const int n_groups = n_tiles * parts;
+  const volatile int* abort = &s.abort;
+
+  // the idx_q rows past a group's tokens stay zero (the copies write only kTok rows)
+  for (int i = threadIdx.x; i < 2 * kIqBytes / 16; i += kThreads)
+    reinterpret_cast<uint4*>(&s.iq[0][0])[i] = make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&s.kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.g_full[i], 1);
+      ptx::mbar_init(&s.g_empty[i], 1);
+    }
+    ptx::mbar_init(&s.s_full, 1);
+    ptx::mbar_init(&s.p_full, 4);
+    ptx::mbar_init(&s.acc_done, 1);
+    ptx::mbar_init(&s.drain, 1);
+    s.abort = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&s.tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::fence_proxy_async_smem();
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+  // TMEM: S^T [0,128) (keys x rows), Z^T [128,128+kNTok) (keys x tokens), gz^T bf16
+  // [192,224), dIK [256,384) (keys x index dims)
+  constexpr uint32_t kColS = 0, kColZ = 128, kColG = 192, kColDK = 256;
+  constexpr uint32_t kIdescZ = ptx::idesc_bf16_f32(128, kNTok, 0, 0);
+
+  if (warp == kProducerWarp) {
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(&s.kv_full, 2 * kTileBytes);
+      for (int kc = 0; kc < 2; ++kc) {
+        ptx::tma_load_3d(s.k + kc * kBk * kRowBytes, &tm_k, &s.kv_full, kc * 64, blk * kBk, bg);
+        ptx::tma_load_3d(s.ik + kc * kBk * kRowBytes, &tm_ik, &s.kv_full, kc * 64, blk * kBk, b);
+      }
+    }
+    for (int gi = 0; gi < n_groups; ++gi) {
+      const int st = gi & 1;
+      if (!ptx::mbar_wait(&s.g_empty[st], ((gi >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+      const int m = s.tiles[gi / parts], part = gi % parts;
+      const int t0 = m * kQt + part * kTok;
+#pragma unroll
+      for (int x4 = 0; x4 < kRows / 32; ++x4) {
+        const int x = x4 * 32 + lane;
+        const int t = t0 + x / G, h = g * G + x % G;
+        s.lse2[st][x] = t < p.Sq ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
+      }
+      for (int x = lane; x < kIqRows; x += 32) {
+        const int t = t0 + x;
+        s.lseI2[st][x] = x < kTok && t < p.Sq ? lse_i[((size_t)b * p.Hkv + g) * p.Sq + t] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&s.g_full[st], kTileBytes + 2 * kTok * kRowBytes);
+        for (int kc = 0; kc < 2; ++kc) {
+          ptx::tma_load_4d(s.q[st] + kc * kRows * kRowBytes, &tm_q, &s.g_full[st], kc * 64,
+                           g * G, t0, b);
+          ptx::tma_load_4d(s.iq[st] + kc * kIqRows * kRowBytes, &tm_iq, &s.g_full[st], kc * 64,
+                           g, t0, b);
+        }
+      }
+      issued = gi + 1;
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x711);
+    if (*abort && lane == 0) {
+      ptx::mbar_wait_timed(&s.kv_full, 0);
+      for (int gi = issued > 2 ? issued - 2 : 0; gi < issued; ++gi)
+        ptx::mbar_wait_timed(&s.g_full[gi & 1], (gi >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp) {
+    bool ok = ptx::mbar_wait(&s.kv_full, 0, abort);
+    bool issued_any = false;
+    const uint32_t ka = ptx::smem_u32(s.k), ia = ptx::smem_u32(s.ik);
+    for (int gi = 0; ok && gi < n_groups; ++gi) {
+      const int st = gi & 1;
+      if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if (lane == 0) {
+        mma_kk(tmem + kColS, ka, ptx::smem_u32(s.q[st]), kRows * kRowBytes, kIdescKK);
+        mma_kk(tmem + kColZ, ia, ptx::smem_u32(s.iq[st]), kIqRows * kRowBytes, kIdescZ);
+        ptx::umma_commit(&s.s_full);
+      }
+      issued_any = true;
+      __syncwarp();
+      if (!ptx::mbar_wait(&s.p_full, gi & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if (lane == 0) {
+        // dIK += gz^T (keys x tokens, TMEM) idx_q (tokens x index dims, MN-major B)
+#pragma unroll
+        for (int kk = 0; kk < kNTok / 16; ++kk)
+          ptx::umma_bf16_ts(tmem + kColDK, tmem + kColG + kk * 8,
+                            ptx::smem_desc_mn_sw128(ptx::smem_u32(s.iq[st]) + kk * 16 * kRowBytes,
+                                                    kIqRows * kRowBytes, 1024),
+                            kIdescMN, (gi > 0 || kk > 0) ? 1u : 0u);
+        ptx::umma_commit(&s.acc_done);
+        ptx::umma_commit(&s.g_empty[st]);
+      }
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x712);
+    if (*abort && lane == 0 && issued_any) {
+      ptx::umma_commit(&s.drain);
+      ptx::mbar_wait_timed(&s.drain, 0);
+    }
+  } else {
+    // --------------------------------------- math warps 0-3: one key of the block each
+    const int key = blk * kBk + warp * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
+    bool ok = true;
+    for (int gi = 0; gi < n_groups; ++gi) {
+      const int st = gi & 1;
+      const int m = s.tiles[gi / parts], part = gi % parts;
+      const int t0 = m * kQt + part * kTok;
+      if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
+          !ptx::mbar_wait(&s.s_full, gi & 1, abort) ||
+          // the previous group's d idx_k MMA has read gz^T
+          (gi > 0 && !ptx::mbar_wait(&s.acc_done, (gi - 1) & 1, abort))) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      float pt[kTok];
+#pragma unroll
+      for (int x = 0; x < kTok; ++x) pt[x] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32];
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int x = c * 32 + e, tok = x / G;
+          if (key <= t0 + tok)
+            pt[tok] += ex2(fmaf(__uint_as_float(sv[e]), c1, -s.lse2[st][x]));
+        }
+      }
+      uint32_t zv[kNTok];
+#pragma unroll
+      for (int c = 0; c < kNTok / 16; ++c) {
+        uint32_t z16[16];
+        ptx::tmem_ld_x16(tmem + lane_off + kColZ + c * 16, z16);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) zv[c * 16 + e] = z16[e];
+      }
+      uint32_t pk[32];
+#pragma unroll
+      for (int x = 0; x < 32; ++x) pk[x] = 0u;
+#pragma unroll
+      for (int tok = 0; tok < kTok; tok += 2) {
+        float gz2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < 2 && tok + u < kTok; ++u) {
+          const bool vis = key <= t0 + tok + u && t0 + tok + u < p.Sq;
+          const float pi =
+              vis ? ex2(fmaf(__uint_as_float(zv[tok + u]), c2, -s.lseI2[st][tok + u])) : 0.f;
+          gz2[u] = pi - pt[tok + u] * (1.f / G);
+        }
+        pk[tok >> 1] = pack_bf16x2(gz2[0], gz2[1]);
+      }
+      ptx::tmem_st_x16(tmem + lane_off + kColG, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      ptx::tmem_st_x16(tmem + lane_off + kColG + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      ptx::tmem_st_wait();
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.p_full);
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x713);
+    const bool have = ok && ptx::mbar_wait(&s.acc_done, (n_groups - 1) & 1, abort);
+    if (have) {
+      ptx::tc_fence_after_sync();
+      const bool in_range = key < p.Sk;
+      float4* dst = reinterpret_cast<float4*>(d_idx_k + ((size_t)b * p.Sk + (in_range ? key : 0)) * kD);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t a[32];
+        ptx::tmem_ld_x32(tmem + lane_off + kColDK + c * 32, a);
+        ptx::tmem_ld_wait();
+        if (in_range) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            atomicAdd(dst + c * 8 + e / 4,
+                      make_float4(__uint_as_float(a[e]) * p.index_scale,
+                                  __uint_as_float(a[e + 1]) * p.index_scale,
+                                  __uint_as_float(a[e + 2]) * p.index_scale,
+                                  __uint_as_float(a[e + 3]) * p.index_scale));
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int G>
+cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tik, const void* idx_q, const int32_t* sel,
+                         const float* lse, float* loss, float* d_idx_q, float* d_idx_k,
+                         float* lse_i, uint32_t* bits, cudaStream_t st, int* status) {
+  CUtensorMap tiq;
+  // idx_q [B, T, Hkv, dI] as (dI, Hkv, T, B); one box = 64 dims x 1 head x (128 / G) tokens
+  const uint64_t qd[4] = {(uint64_t)kD, (uint64_t)p.Hkv, (uint64_t)p.Sq, (uint64_t)p.B};
+  const uint64_t qs[3] = {(uint64_t)kD * 2, (uint64_t)p.Hkv * kD * 2,
+                          (uint64_t)p.Sq * p.Hkv * kD * 2};
+  const uint32_t qb[4] = {64, 1, (uint32_t)(kRows / G), 1};
+  cudaError_t e = make_tensor_map_bf16(&tiq, idx_q, 4, qd, qs, qb);
+  if (e != cudaSuccess) return e;
+  {
+    auto kern = kl_rows_tc_kernel<G>;
+    const size_t smem = sizeof(SmemR) + 1024;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.Qt * G / kRows, p.nR, p.B * p.Hkv);
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, (const __nv_bfloat16*)idx_q, sel, lse, lse_i,
+                                       loss, d_idx_q, p, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    auto kern = kl_keys_tc_kernel<G>;
+    const size_t smem = sizeof(SmemK) + 1024;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int words = (p.nR + 31) / 32;
+    const int wpc = tiles_per_cta(p) / 32;
+    dim3 grid((words + wpc - 1) / wpc, p.nB, p.B * p.Hkv);
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, tiq, bits, lse, lse_i, d_idx_k, p, words,
+                                       wpc, status);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+bool index_kl_tc_supported(const Dims& p) {
+  return p.dtype == 1 && !p.decode && p.d == kD && p.dI == kD && p.Bk == kBk && p.Qt == kQt &&
+         (p.G == 2 || p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32) && p.k <= kMaxSel;
+}
+
+size_t index_kl_tc_workspace_bytes(const Dims& p) {
+  const size_t lse_i = ((size_t)p.B * p.Hkv * p.Sq * sizeof(float) + 255) / 256 * 256;
+  const size_t words = (size_t)(p.nR + 31) / 32;
+  return lse_i + (size_t)p.B * p.Hkv * p.nB * words * sizeof(uint32_t);
+}
+
+cudaError_t launch_index_kl_tc(const Dims& p, const void* q, const void* k, const float* lse,
+                               const void* idx_q, const void* idx_k, const int32_t* sel,
+                               float* loss, float* d_idx_q, float* d_idx_k, void* workspace,
+                               cudaStream_t st, int* status) {
+  const size_t lse_i_bytes = ((size_t)p.B * p.Hkv * p.Sq * sizeof(float) + 255) / 256 * 256;
+  float* lse_i = reinterpret_cast<float*>(workspace);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + lse_i_bytes);
+  cudaError_t e = cudaMemsetAsync(loss, 0, sizeof(float), st);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(d_idx_k, 0, (size_t)p.B * p.Sk * kD * sizeof(float), st);
+  if (e != cudaSuccess) return e;
+  if ((e = launch_selection_bitmap(p, sel, bits, st)) != cudaSuccess) return e;
+
+  CUtensorMap tq, tk, tik;
+  const uint64_t qd[4] = {(uint64_t)kD, (uint64_t)p.Hq, (uint64_t)p.Sq, (uint64_t)p.B};
+  const uint64_t qs[3] = {(uint64_t)kD * 2, (uint64_t)p.Hq * kD * 2,
+                          (uint64_t)p.Sq * p.Hq * kD * 2};
+  const uint32_t qb[4] = {64, (uint32_t)p.G, (uint32_t)(kRows / p.G), 1};
+  const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)p.Sk, (uint64_t)p.B * p.Hkv};
+  const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)p.Sk * kD * 2};
+  const uint32_t kb[3] = {64, (uint32_t)kBk, 1};
+  // idx_k [B, T, dI] as (dI, T, B)
+  const uint64_t ikd[3] = {(uint64_t)kD, (uint64_t)p.Sk, (uint64_t)p.B};
+  e = make_tensor_map_bf16(&tq, q, 4, qd, qs, qb);
+  if (e == cudaSuccess) e = make_tensor_map_bf16(&tk, k, 3, kd, ks, kb);
+  if (e == cudaSuccess) e = make_tensor_map_bf16(&tik, idx_k, 3, ikd, ks, kb);
+  if (e != cudaSuccess) return e;
+  switch (p.G) {
+    case 2: return launch_kl_tc<2>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
+    case 4: return launch_kl_tc<4>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
+    case 8: return launch_kl_tc<8>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
+    case 16: return launch_kl_tc<16>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
+    default: return launch_kl_tc<32>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
+  }
+}
+
+}  // namespace msa

@@ -242,7 +242,7 @@ msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, co
 msa_status msa_index_kl_loss(const msa_shape* shape, const void* q, const void* k,
                              const float* lse, const void* idx_q, const void* idx_k,
                              const int32_t* sel, float* loss, float* d_idx_q, float* d_idx_k,
-                             void* stream) {
+                             void* workspace, size_t ws_bytes, void* stream) {
   g_last_error[0] = 0;
   Dims d;
   MSA_TRY(make_dims(shape, &d));
@@ -258,8 +258,14 @@ msa_status msa_index_kl_loss(const msa_shape* shape, const void* q, const void* 
   MSA_TRY(check_ptr(loss, "loss"));
   MSA_TRY(check_ptr(d_idx_q, "d_idx_q"));
   MSA_TRY(check_ptr(d_idx_k, "d_idx_k"));
+  const size_t need = index_kl_workspace_bytes(d);
+  if (need > 0) {
+    MSA_TRY(check_ptr(workspace, "workspace"));
+    if (ws_bytes < need)
+      return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, need);
+  }
   cudaError_t e = launch_index_kl(d, q, k, lse, idx_q, idx_k, sel, loss, d_idx_q, d_idx_k,
-                                  (cudaStream_t)stream);
+                                  workspace, (cudaStream_t)stream, status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_kl_loss launch");
 }
 
@@ -371,6 +377,7 @@ size_t msa_workspace_bytes(const msa_shape* shape, int which) {
   if (make_dims(shape, &d) != MSA_OK) return 0;
   if (which == 1 && d.decode) return decode_workspace_bytes(d);
   if (which == 2 && !d.decode) return backward_workspace_bytes(d);
+  if (which == 3 && !d.decode) return index_kl_workspace_bytes(d);
   return 0;
 }
 

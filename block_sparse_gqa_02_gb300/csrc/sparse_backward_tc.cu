@@ -605,15 +605,27 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
 }
 
-// Query tiles per dK/dV CTA: about nR / 16 (so a block every tile selected is split over
-// ~16 CTAs), a multiple of 32 between 32 and kMaxTilesPerCta.
+}  // namespace
+
+cudaError_t launch_selection_bitmap(const Dims& p, const int32_t* sel, uint32_t* bits,
+                                   cudaStream_t st) {
+  const int words = (p.nR + 31) / 32;
+  cudaError_t e = cudaMemsetAsync(bits, 0, (size_t)p.B * p.Hkv * p.nB * words * sizeof(uint32_t),
+                                  st);
+  if (e != cudaSuccess) return e;
+  const size_t n = (size_t)p.B * p.Hkv * p.nR * p.k;
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  selection_bitmap_kernel<<<blocks, 256, 0, st>>>(sel, bits, p, words);
+  return cudaGetLastError();
+}
+
+// Query tiles per key-block CTA: about nR / 16 (so a block every tile selected is split
+// over ~16 CTAs), a multiple of 32 between 32 and kMaxTilesPerCta.
 int tiles_per_cta(const Dims& p) {
   int t = (p.nR + 15) / 16;
   t = (t + 31) / 32 * 32;
   return t < 32 ? 32 : (t > kMaxTilesPerCta ? kMaxTilesPerCta : t);
 }
-
-}  // namespace
 
 bool sparse_backward_tc_supported(const Dims& p) {
   return p.dtype == 1 && !p.decode && p.d == kD && p.Bk == kBk && p.Qt == kQt && p.G >= 2 &&
@@ -635,11 +647,9 @@ cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* 
   float* dvec = reinterpret_cast<float*>(workspace);
   uint32_t* bits = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + dvec_bytes);
   const int words = (p.nR + 31) / 32;
-  const size_t bitmap_bytes = (size_t)p.B * p.Hkv * p.nB * words * sizeof(uint32_t);
   const size_t kv_bytes = (size_t)p.B * p.Hkv * p.Sk * kD * sizeof(float);
   cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(dv, 0, kv_bytes, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(bits, 0, bitmap_bytes, st);
   if (e != cudaSuccess) return e;
 
   CUtensorMap tq, tdo, tk, tv;
@@ -658,12 +668,7 @@ cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* 
   if (e == cudaSuccess) e = make_tensor_map_bf16(&tv, v, 3, kd, ks, kb);
   if (e != cudaSuccess) return e;
 
-  {
-    const size_t n = (size_t)p.B * p.Hkv * p.nR * p.k;
-    const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    selection_bitmap_kernel<<<blocks, 256, 0, st>>>(sel, bits, p, words);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
+  if ((e = launch_selection_bitmap(p, sel, bits, st)) != cudaSuccess) return e;
   {
     const size_t smem = sizeof(SmemQ) + 1024;
     e = cudaFuncSetAttribute(backward_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

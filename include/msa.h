@@ -155,11 +155,16 @@ msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, co
  * Outputs, float32: loss (one device scalar, cleared then accumulated), d_idx_q [batch,
  * seq_q, n_heads_kv, index_dim] (written), d_idx_k [batch, seq_k, index_dim] (cleared, then
  * accumulated over every tile and head): the gradients of loss.  Prefill shapes, at most
- * 64 query heads per KV head.  CUDA cores, fp32. */
+ * 64 query heads per KV head.  bf16 shapes with head_dim = index_dim = 128, block 128,
+ * q_tile 64 and 2, 4, 8, 16 or 32 query heads per KV head run on the tensor cores (a
+ * query-tile pass for the loss and d_idx_q, a key-block pass for d_idx_k) and need a
+ * device workspace of msa_workspace_bytes(shape, 3) bytes; other shapes run on CUDA cores
+ * in fp32 and need none.  d_idx_k and the loss are sums with fp32 atomics, so their last
+ * bits can vary from run to run. */
 msa_status msa_index_kl_loss(const msa_shape* shape, const void* q, const void* k,
                              const float* lse, const void* idx_q, const void* idx_k,
                              const int32_t* sel, float* loss, float* d_idx_q, float* d_idx_k,
-                             void* stream);
+                             void* workspace, size_t ws_bytes, void* stream);
 
 /* Main branch, decode (seq_q == 1, q_tile == 1): the new token of every sequence attends
  * over the selected blocks of the cache (split over the blocks, partial results merged by
@@ -220,9 +225,9 @@ msa_status msa_sparse_decode_paged(const msa_shape* shape, const int32_t* seq_le
                                    void* out, float* lse, void* workspace, size_t ws_bytes,
                                    void* stream);
 
-/* Scratch bytes msa_sparse_prefill (which = 0), msa_sparse_decode (which = 1) or
- * msa_sparse_prefill_backward (which = 2) needs for this shape; 0 when none.  Returns 0
- * for an invalid shape. */
+/* Scratch bytes msa_sparse_prefill (which = 0), msa_sparse_decode (which = 1),
+ * msa_sparse_prefill_backward (which = 2) or msa_index_kl_loss (which = 3) needs for this
+ * shape; 0 when none.  Returns 0 for an invalid shape. */
 size_t msa_workspace_bytes(const msa_shape* shape, int which);
 
 /* Synchronises `stream`, then reports (and clears) the device status word and any pending

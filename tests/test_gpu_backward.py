@@ -62,6 +62,12 @@ KL_CASES = {
                                                n_heads_q=64, top_k=6, block_size=64),
     "bf16_4096_k16": CONFIGS["p32k"].with_(seq=4096, n_plants=5),
     "bf16_qt128_ragged": CONFIGS["p32k"].with_(seq=1500, q_tile=128, top_k=4, n_plants=2),
+    # tensor-core path: G = 2, 4, 16, 32; and blocks shared by the tiles of several CTAs
+    "bf16_g16_3000": CONFIGS["p32k"].with_(seq=3000, n_heads_q=64, top_k=8, n_plants=3),
+    "bf16_g4_k1": CONFIGS["p32k"].with_(seq=1200, n_heads_q=16, top_k=1, n_plants=0),
+    "bf16_g2_ragged": CONFIGS["p32k"].with_(seq=700, n_heads_q=8, top_k=3, n_plants=0),
+    "bf16_g32_ragged": CONFIGS["p32k"].with_(seq=900, n_heads_q=128, top_k=3, n_plants=0),
+    "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=4),
 }
 
 
@@ -80,12 +86,20 @@ def test_index_kl_loss(name):
     loss = torch.full((1,), float("nan"), device="cuda")
     diq = torch.full(x["idx_q"].shape, float("nan"), device="cuda")
     dik = torch.full(x["idx_k"].shape, float("nan"), device="cuda")
+    ws_bytes = _lib.msa_workspace_bytes(shape, 3)
+    ws = torch.full((ws_bytes // 4 + 1,), float("nan"), device="cuda") if ws_bytes else None
     _lib.msa_index_kl_loss(shape, x["q"], x["k"], lse, x["idx_q"], x["idx_k"], sel, loss,
-                           diq, dik)
+                           diq, dik, ws)
     _lib.msa_get_device_status()
     ref_loss, ref_q, ref_k = oracle.index_kl_loss(x["q"], x["k"], x["idx_q"], x["idx_k"],
                                                   sel_np, cfg.block_size, cfg.q_tile)
-    assert abs(loss.item() - ref_loss) <= 1e-3 * abs(ref_loss), (loss.item(), ref_loss)
     tol = "f32" if cfg.dtype == "f32" else "bf16"
     check_grad(diq, ref_q, tol, f"{name} d idx_q")
     check_grad(dik, ref_k, tol, f"{name} d idx_k")
+    # the loss sums one KL per (token, KV head); each is evaluated in fp32 from normalised
+    # probabilities whose sum is 1 only to fp32 rounding, which leaves an absolute error of
+    # order 1e-7 per term: near-uniform inputs give KLs of that order, so the bound has an
+    # absolute part per term beside the relative one
+    n_terms = cfg.batch * cfg.seq * cfg.n_heads_kv
+    assert abs(loss.item() - ref_loss) <= 1e-3 * abs(ref_loss) + 1e-6 * n_terms, \
+        (loss.item(), ref_loss)
