@@ -16,12 +16,14 @@
 //   pass over the blocks forms lseI2 from Z = idx_q idx_k^T, with each row's idx_q replicated
 //   so that every row of a token holds its token's index logits; a second pass forms S and Z
 //   again, the math warps average the G rows of a token with warp shuffles, accumulate the
-//   loss and write gz into TMEM, and d idx_q += gz idx_k accumulates in TMEM.
+//   loss and write gz into TMEM, and d idx_q += gz idx_k accumulates in TMEM.  It leaves each
+//   128-row group's main lse2 (per row) and lseI2 (per token) as one 1 KiB record.
 // * keys (key-block order over the tiles that selected the block, as in the dK/dV pass of
 //   the backward): S^T = K Q^T and Z^T = idx_k idx_q^T with the keys on the TMEM lanes, so a
 //   token's G rows are adjacent columns; gz^T goes to TMEM and d idx_k += gz^T idx_q
 //   accumulates there over all of the CTA's groups before one set of vector atomics.
-// Every wait is bounded.
+// Warps: 8 elementwise warps (two per TMEM lane quadrant, each taking half of the columns),
+// a TMA producer and an MMA issuer.  Every wait is bounded.
 #include "common.cuh"
 #include "index_kl_tc.cuh"
 #include "ptx.cuh"
@@ -39,8 +41,9 @@ constexpr int kRows = 128;
 constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;           // [2 chunks][128 rows][128 B]
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 192;                               // 4 math warps, producer, MMA
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kThreads = 320;                               // 8 math warps, producer, MMA
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kMathWarps = 8;                               // two per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);
@@ -72,6 +75,12 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_smem, uint32_
   }
 }
 
+// Column of bf16 chunk c (32 values packed into 16 columns) written over an fp32 region of
+// 128 columns: chunks 0-1 over the region's columns 0-31, chunks 2-3 over 96-127, so each of
+// the two warps of a lane quadrant (columns 0-63 / 64-127) overwrites only columns it has
+// itself loaded.
+__device__ __forceinline__ int p_col(int c) { return c < 2 ? c * 16 : 96 + (c - 2) * 16; }
+
 __device__ __forceinline__ void raise_abort(int* abort_flag, int* status, int code) {
   *abort_flag = 1;
   if (status) atomicExch(status, code);
@@ -87,6 +96,7 @@ struct __align__(1024) SmemR {
   uint64_t q_full, ring_full[2], ring_empty[2];
   uint64_t z_full[2], z_free[2], pass1_done;
   uint64_t s_full, g_full, dq_done, drain;
+  float half_ml[2][2][kRows];   // pass 1: [column half][max, sum][row]
   int blocks[kMaxSel];
   int n_sel;
   uint32_t tmem_base;
@@ -98,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ik,
                   const __nv_bfloat16* __restrict__ idx_q, const int32_t* __restrict__ sel,
-                  const float* __restrict__ lse, float* __restrict__ lse_i, float* __restrict__ loss,
+                  const float* __restrict__ lse, float* __restrict__ rowstat, float* __restrict__ loss,
                   float* __restrict__ d_idx_q, Dims p, int* status) {
   extern __shared__ uint8_t smem_raw[];
   SmemR& s = *reinterpret_cast<SmemR*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -117,11 +127,11 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_init(&s.ring_full[i], 1);
       ptx::mbar_init(&s.ring_empty[i], 1);
       ptx::mbar_init(&s.z_full[i], 1);
-      ptx::mbar_init(&s.z_free[i], 4);
+      ptx::mbar_init(&s.z_free[i], kMathWarps);
     }
-    ptx::mbar_init(&s.pass1_done, 4);
+    ptx::mbar_init(&s.pass1_done, kMathWarps);
     ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.g_full, 4);
+    ptx::mbar_init(&s.g_full, kMathWarps);
     ptx::mbar_init(&s.dq_done, 1);
     ptx::mbar_init(&s.drain, 1);
     s.abort = 0;
@@ -233,10 +243,11 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ptx::mbar_wait(&s.g_full, j & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       if (lane == 0) {
-        // dIQ += gz idx_k: gz (rows x keys) from TMEM, idx_k as the MN-major B operand
+        // dIQ += gz idx_k: gz (rows x keys) from TMEM (keys 64-127 at columns 96-127),
+        // idx_k as the MN-major B operand
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          ptx::umma_bf16_ts(tmem + kColDQ, tmem + kColS + kk * 8,
+          ptx::umma_bf16_ts(tmem + kColDQ, tmem + kColS + kk * 8 + (kk >= 4 ? 64 : 0),
                             ptx::smem_desc_mn_sw128(ptx::smem_u32(s.ik[st]) + kk * 16 * kRowBytes,
                                                     kBk * kRowBytes, 1024),
                             kIdescMN, (j > 0 || kk > 0) ? 1u : 0u);
@@ -251,80 +262,107 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_wait_timed(&s.drain, 0);
     }
   } else {
-    // ------------------------------------------------ math warps 0-3: one row each
-    const int r = warp * 32 + lane;
+    // ------------------------- math warps 0-7: warp w takes row quadrant w % 4 and the key
+    // columns (and d idx_q columns) 64 (w / 4) .. +63
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;
     const int t = t0 + r / G, hh = r % G, h = g * G + hh;
     const bool valid = t < p.Sq;
     const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     bool ok = true;
-    // pass 1: log2-sum-exp of the index logits over the tile's visible keys
+    // pass 1: log2-sum-exp of the index logits over the tile's visible keys (this warp's
+    // half of the columns, then combined with the other half's)
     float mI = -INFINITY, lI = 0.f;
     for (int j = 0; j < n_sel; ++j) {
       const int buf = j & 1, lim = t - s.blocks[j] * kBk;
       if (!ptx::mbar_wait(&s.z_full[buf], (j >> 1) & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t zv[32];
-        ptx::tmem_ld_x32(tmem + lane_off + buf * 128 + c * 32, zv);
-        ptx::tmem_ld_wait();
+      uint32_t zv[2][32];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        ptx::tmem_ld_x32(tmem + lane_off + buf * 128 + (2 * half + u) * 32, zv[u]);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.z_free[buf]);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = 2 * half + u;
         float cm = -INFINITY;
 #pragma unroll
         for (int e = 0; e < 32; ++e)
-          if (c * 32 + e <= lim) cm = fmaxf(cm, __uint_as_float(zv[e]) * c2);
+          if (c * 32 + e <= lim) cm = fmaxf(cm, __uint_as_float(zv[u][e]) * c2);
         if (cm != -INFINITY) {
           const float mn = fmaxf(mI, cm);
           float acc = 0.f;
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= lim) acc += ex2(fmaf(__uint_as_float(zv[e]), c2, -mn));
+            if (c * 32 + e <= lim) acc += ex2(fmaf(__uint_as_float(zv[u][e]), c2, -mn));
           lI = lI * ex2(mI - mn) + acc;
           mI = mn;
         }
       }
-      ptx::tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s.z_free[buf]);
+    }
+    // every math warp reaches this barrier exactly once (also after a failed wait)
+    s.half_ml[half][0][r] = mI;
+    s.half_ml[half][1][r] = lI;
+    asm volatile("bar.sync 1, %0;" ::"r"(kMathWarps * 32) : "memory");
+    {
+      const float mo = s.half_ml[half ^ 1][0][r], lo = s.half_ml[half ^ 1][1][r];
+      const float mn = fmaxf(mI, mo);
+      if (mn != -INFINITY) {
+        lI = lI * ex2(mI - mn) + lo * ex2(mo - mn);
+        mI = mn;
+      }
     }
     const float lseI2 = mI == -INFINITY ? -INFINITY : mI + __log2f(lI);
-    if (ok && valid && hh == 0) lse_i[((size_t)b * p.Hkv + g) * p.Sq + t] = lseI2;
     ptx::tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&s.pass1_done);
     // pass 2: target, loss, gz
     const float lse2 = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
+    if (half == 0) {
+      // the group's record for the key-block pass: lse2 per row, then lseI2 per token
+      float* rec = rowstat + (((size_t)bg * p.nR + m) * gridDim.x + part) * 2 * kRows;
+      rec[r] = lse2;
+      if (hh == 0) rec[kRows + r / G] = lseI2;
+    }
     float lsum = 0.f;
     for (int j = 0; ok && j < n_sel; ++j) {
       const int lim = t - s.blocks[j] * kBk;
       if (!ptx::mbar_wait(&s.s_full, j & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], zv[32];
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
-        ptx::tmem_ld_x32(tmem + lane_off + kColZ + c * 32, zv);
-        ptx::tmem_ld_wait();
+      uint32_t sv[2][32], zv[2][32];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + kColZ + (2 * half + u) * 32, zv[u]);
+      }
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = 2 * half + u;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float gz2[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const bool vis = c * 32 + e + u <= lim;
-            float pt = vis ? ex2(fmaf(__uint_as_float(sv[e + u]), c1, -lse2)) : 0.f;
+          for (int w = 0; w < 2; ++w) {
+            const bool vis = c * 32 + e + w <= lim;
+            float pt = vis ? ex2(fmaf(__uint_as_float(sv[u][e + w]), c1, -lse2)) : 0.f;
 #pragma unroll
             for (int o = 1; o < G; o <<= 1) pt += __shfl_xor_sync(0xffffffffu, pt, o);
             pt *= 1.f / G;
-            const float zl = fmaf(__uint_as_float(zv[e + u]), c2, -lseI2);   // log2 p_I
+            const float zl = fmaf(__uint_as_float(zv[u][e + w]), c2, -lseI2);   // log2 p_I
             const float pi = vis ? ex2(zl) : 0.f;
             if (hh == 0 && pt > 0.f) lsum += pt * (__log2f(pt) - zl);
-            gz2[u] = pi - pt;
+            gz2[w] = pi - pt;
           }
           pk[e >> 1] = pack_bf16x2(gz2[0], gz2[1]);
         }
-        // gz chunk c over S columns 16c .. 16c+15 (already loaded)
-        ptx::tmem_st_x16(tmem + lane_off + kColS + c * 16, pk);
+        // gz over S columns this warp loaded (p_col)
+        ptx::tmem_st_x16(tmem + lane_off + kColS + p_col(c), pk);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
@@ -336,7 +374,8 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (have) ptx::tc_fence_after_sync();
     float* dst = d_idx_q + (((size_t)b * p.Sq + (valid ? t : 0)) * p.Hkv + g) * kD;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int u = 0; u < 2; ++u) {
+      const int c = 2 * half + u;
       uint32_t v[32];
       if (have) {
         ptx::tmem_ld_x32(tmem + lane_off + kColDQ + c * 32, v);
@@ -353,7 +392,7 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                    : make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    // the loss of this warp's rows (one lane per token), natural log
+    // the loss of this warp's rows and columns (one lane per token), natural log
     float lv = lsum * kLn2;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
@@ -378,8 +417,7 @@ struct __align__(1024) SmemK {
   uint8_t ik[kTileBytes];
   uint8_t q[2][kTileBytes];
   uint8_t iq[2][kIqBytes];
-  float lse2[2][kRows];
-  float lseI2[2][kIqRows];
+  float rec[2][2 * kRows];     // a group's lse2 per row [0,128), lseI2 per token [128,..)
   uint64_t kv_full, g_full[2], g_empty[2];
   uint64_t s_full, p_full, acc_done, drain;
   int tiles[kMaxTilesPerCta];
@@ -392,8 +430,8 @@ template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
 kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ik, const __grid_constant__ CUtensorMap tm_iq,
-                  const uint32_t* __restrict__ bits, const float* __restrict__ lse,
-                  const float* __restrict__ lse_i, float* __restrict__ d_idx_k, Dims p, int words,
+                  const uint32_t* __restrict__ bits, const float* __restrict__ rowstat,
+                  float* __restrict__ d_idx_k, Dims p, int words,
                   int words_per_cta, int* status) {
   extern __shared__ uint8_t smem_raw[];
   SmemK& s = *reinterpret_cast<SmemK*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -441,7 +479,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_init(&s.g_empty[i], 1);
     }
     ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.p_full, 4);
+    ptx::mbar_init(&s.p_full, kMathWarps);
     ptx::mbar_init(&s.acc_done, 1);
     ptx::mbar_init(&s.drain, 1);
     s.abort = 0;
@@ -476,19 +514,10 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       if (!ptx::mbar_wait(&s.g_empty[st], ((gi >> 1) & 1) ^ 1, abort)) { ok = false; break; }
       const int m = s.tiles[gi / parts], part = gi % parts;
       const int t0 = m * kQt + part * kTok;
-#pragma unroll
-      for (int x4 = 0; x4 < kRows / 32; ++x4) {
-        const int x = x4 * 32 + lane;
-        const int t = t0 + x / G, h = g * G + x % G;
-        s.lse2[st][x] = t < p.Sq ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
-      }
-      for (int x = lane; x < kIqRows; x += 32) {
-        const int t = t0 + x;
-        s.lseI2[st][x] = x < kTok && t < p.Sq ? lse_i[((size_t)b * p.Hkv + g) * p.Sq + t] : 0.f;
-      }
-      __syncwarp();
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&s.g_full[st], kTileBytes + 2 * kTok * kRowBytes);
+        ptx::mbar_arrive_expect_tx(&s.g_full[st], kTileBytes + 2 * kTok * kRowBytes + 2 * kRows * 4);
+        ptx::bulk_load(s.rec[st], rowstat + (((size_t)bg * p.nR + m) * parts + part) * 2 * kRows,
+                       2 * kRows * 4, &s.g_full[st]);
         for (int kc = 0; kc < 2; ++kc) {
           ptx::tma_load_4d(s.q[st] + kc * kRows * kRowBytes, &tm_q, &s.g_full[st], kc * 64,
                            g * G, t0, b);
@@ -541,10 +570,25 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_wait_timed(&s.drain, 0);
     }
   } else {
-    // --------------------------------------- math warps 0-3: one key of the block each
-    const int key = blk * kBk + warp * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ----------------- math warps 0-7: one key of the block per lane (quadrant w % 4); warp
+    // w takes the group rows 64 (w / 4) .. +63, i.e. tokens kTok / 2 (w / 4) .. +kTok / 2, and
+    // the d idx_k columns 64 (w / 4) .. +63
+    constexpr int kHalfTok = kTok / 2;
+    const int quad = warp & 3, half = warp >> 2;
+    const int key = blk * kBk + quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
+    if (half == 0 && kHalfTok < 32) {
+      // gz^T columns past the group's tokens (the padding up to the UMMA's 16) stay zero
+      const uint32_t zero[16] = {};
+      for (int c0 = kHalfTok; c0 < 32; c0 += 16) {
+        uint32_t z16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) z16[e] = zero[e];
+        ptx::tmem_st_x16(tmem + lane_off + kColG + c0, z16);
+      }
+      ptx::tmem_st_wait();
+    }
     bool ok = true;
     for (int gi = 0; gi < n_groups; ++gi) {
       const int st = gi & 1;
@@ -555,47 +599,54 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // the previous group's d idx_k MMA has read gz^T
           (gi > 0 && !ptx::mbar_wait(&s.acc_done, (gi - 1) & 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      float pt[kTok];
+      uint32_t sv[2][32];
 #pragma unroll
-      for (int x = 0; x < kTok; ++x) pt[x] = 0.f;
+      for (int u = 0; u < 2; ++u)
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
+      // this warp's tokens' Z^T columns (loaded 16 at a time; a 16-column load that runs past
+      // the Z^T columns reads unused TMEM and those values are not used)
+      constexpr int kZLoads = kHalfTok < 16 ? 1 : kHalfTok / 16;
+      uint32_t zv[kZLoads][16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32];
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
-        ptx::tmem_ld_wait();
+      for (int c = 0; c < kZLoads; ++c)
+        ptx::tmem_ld_x16(tmem + lane_off + kColZ + half * kHalfTok + c * 16, zv[c]);
+      ptx::tmem_ld_wait();
+      float pt[kHalfTok];
+#pragma unroll
+      for (int x = 0; x < kHalfTok; ++x) pt[x] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int x = c * 32 + e, tok = x / G;
-          if (key <= t0 + tok)
-            pt[tok] += ex2(fmaf(__uint_as_float(sv[e]), c1, -s.lse2[st][x]));
+          const int x = half * 64 + u * 32 + e;              // row of the group
+          const int tok = (u * 32 + e) / G;                  // this warp's token index
+          if (key <= t0 + half * kHalfTok + tok)
+            pt[tok] += ex2(fmaf(__uint_as_float(sv[u][e]), c1, -s.rec[st][x]));
         }
-      }
-      uint32_t zv[kNTok];
+      uint32_t pk[16];
 #pragma unroll
-      for (int c = 0; c < kNTok / 16; ++c) {
-        uint32_t z16[16];
-        ptx::tmem_ld_x16(tmem + lane_off + kColZ + c * 16, z16);
-        ptx::tmem_ld_wait();
+      for (int x = 0; x < 16; ++x) pk[x] = 0u;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) zv[c * 16 + e] = z16[e];
-      }
-      uint32_t pk[32];
+      for (int tk = 0; tk < kHalfTok; tk += 2) {
+        float gz2[2];
 #pragma unroll
-      for (int x = 0; x < 32; ++x) pk[x] = 0u;
-#pragma unroll
-      for (int tok = 0; tok < kTok; tok += 2) {
-        float gz2[2] = {0.f, 0.f};
-#pragma unroll
-        for (int u = 0; u < 2 && tok + u < kTok; ++u) {
-          const bool vis = key <= t0 + tok + u && t0 + tok + u < p.Sq;
-          const float pi =
-              vis ? ex2(fmaf(__uint_as_float(zv[tok + u]), c2, -s.lseI2[st][tok + u])) : 0.f;
-          gz2[u] = pi - pt[tok + u] * (1.f / G);
+        for (int u = 0; u < 2; ++u) {
+          const int tok = half * kHalfTok + tk + u;          // token of the group
+          const bool vis = key <= t0 + tok && t0 + tok < p.Sq;
+          const float pi = vis ? ex2(fmaf(__uint_as_float(zv[(tk + u) / 16][(tk + u) % 16]), c2,
+                                          -s.rec[st][kRows + tok]))
+                               : 0.f;
+          gz2[u] = pi - pt[tk + u] * (1.f / G);
         }
-        pk[tok >> 1] = pack_bf16x2(gz2[0], gz2[1]);
+        pk[tk >> 1] = pack_bf16x2(gz2[0], gz2[1]);
       }
-      ptx::tmem_st_x16(tmem + lane_off + kColG, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-      ptx::tmem_st_x16(tmem + lane_off + kColG + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      // this warp's tokens' gz^T columns (2 tokens per column)
+      const uint32_t gcol = tmem + lane_off + kColG + half * (kHalfTok / 2);
+      if constexpr (kHalfTok / 2 == 1) ptx::tmem_st_x1(gcol, pk);
+      else if constexpr (kHalfTok / 2 == 2) ptx::tmem_st_x2(gcol, pk);
+      else if constexpr (kHalfTok / 2 == 4) ptx::tmem_st_x4(gcol, pk);
+      else if constexpr (kHalfTok / 2 == 8) ptx::tmem_st_x8(gcol, pk);
+      else ptx::tmem_st_x16(gcol, pk);
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
       __syncwarp();
@@ -608,7 +659,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool in_range = key < p.Sk;
       float4* dst = reinterpret_cast<float4*>(d_idx_k + ((size_t)b * p.Sk + (in_range ? key : 0)) * kD);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int u = 0; u < 2; ++u) {
+        const int c = 2 * half + u;
         uint32_t a[32];
         ptx::tmem_ld_x32(tmem + lane_off + kColDK + c * 32, a);
         ptx::tmem_ld_wait();
@@ -637,7 +689,7 @@ template <int G>
 cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tik, const void* idx_q, const int32_t* sel,
                          const float* lse, float* loss, float* d_idx_q, float* d_idx_k,
-                         float* lse_i, uint32_t* bits, cudaStream_t st, int* status) {
+                         float* rowstat, uint32_t* bits, cudaStream_t st, int* status) {
   CUtensorMap tiq;
   // idx_q [B, T, Hkv, dI] as (dI, Hkv, T, B); one box = 64 dims x 1 head x (128 / G) tokens
   const uint64_t qd[4] = {(uint64_t)kD, (uint64_t)p.Hkv, (uint64_t)p.Sq, (uint64_t)p.B};
@@ -652,8 +704,8 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.Qt * G / kRows, p.nR, p.B * p.Hkv);
-    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, (const __nv_bfloat16*)idx_q, sel, lse, lse_i,
-                                       loss, d_idx_q, p, status);
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, (const __nv_bfloat16*)idx_q, sel, lse,
+                                       rowstat, loss, d_idx_q, p, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -664,8 +716,8 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
     const int words = (p.nR + 31) / 32;
     const int wpc = tiles_per_cta(p) / 32;
     dim3 grid((words + wpc - 1) / wpc, p.nB, p.B * p.Hkv);
-    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, tiq, bits, lse, lse_i, d_idx_k, p, words,
-                                       wpc, status);
+    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, tiq, bits, rowstat, d_idx_k, p, words, wpc,
+                                       status);
     e = cudaGetLastError();
   }
   return e;
@@ -679,18 +731,19 @@ bool index_kl_tc_supported(const Dims& p) {
 }
 
 size_t index_kl_tc_workspace_bytes(const Dims& p) {
-  const size_t lse_i = ((size_t)p.B * p.Hkv * p.Sq * sizeof(float) + 255) / 256 * 256;
+  // per 128-row group: a 1 KiB record of lse2 / lseI2, then the bitmap
+  const size_t rowstat = (size_t)p.B * p.Hkv * p.nR * (p.Qt * p.G / kRows) * 2 * kRows * 4;
   const size_t words = (size_t)(p.nR + 31) / 32;
-  return lse_i + (size_t)p.B * p.Hkv * p.nB * words * sizeof(uint32_t);
+  return rowstat + (size_t)p.B * p.Hkv * p.nB * words * sizeof(uint32_t);
 }
 
 cudaError_t launch_index_kl_tc(const Dims& p, const void* q, const void* k, const float* lse,
                                const void* idx_q, const void* idx_k, const int32_t* sel,
                                float* loss, float* d_idx_q, float* d_idx_k, void* workspace,
                                cudaStream_t st, int* status) {
-  const size_t lse_i_bytes = ((size_t)p.B * p.Hkv * p.Sq * sizeof(float) + 255) / 256 * 256;
-  float* lse_i = reinterpret_cast<float*>(workspace);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + lse_i_bytes);
+  const size_t rowstat_bytes = (size_t)p.B * p.Hkv * p.nR * (p.Qt * p.G / kRows) * 2 * kRows * 4;
+  float* rowstat = reinterpret_cast<float*>(workspace);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + rowstat_bytes);
   cudaError_t e = cudaMemsetAsync(loss, 0, sizeof(float), st);
   if (e == cudaSuccess)
     e = cudaMemsetAsync(d_idx_k, 0, (size_t)p.B * p.Sk * kD * sizeof(float), st);
@@ -712,11 +765,11 @@ cudaError_t launch_index_kl_tc(const Dims& p, const void* q, const void* k, cons
   if (e == cudaSuccess) e = make_tensor_map_bf16(&tik, idx_k, 3, ikd, ks, kb);
   if (e != cudaSuccess) return e;
   switch (p.G) {
-    case 2: return launch_kl_tc<2>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
-    case 4: return launch_kl_tc<4>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
-    case 8: return launch_kl_tc<8>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
-    case 16: return launch_kl_tc<16>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
-    default: return launch_kl_tc<32>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, lse_i, bits, st, status);
+    case 2: return launch_kl_tc<2>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, rowstat, bits, st, status);
+    case 4: return launch_kl_tc<4>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, rowstat, bits, st, status);
+    case 8: return launch_kl_tc<8>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, rowstat, bits, st, status);
+    case 16: return launch_kl_tc<16>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, rowstat, bits, st, status);
+    default: return launch_kl_tc<32>(p, tq, tk, tik, idx_q, sel, lse, loss, d_idx_q, d_idx_k, rowstat, bits, st, status);
   }
 }
 

@@ -5,8 +5,8 @@
 
 namespace msa {
 bool index_kl_tc_supported(const Dims& p);
-// scratch: the index log2-normaliser per (sequence, KV head, token), then the bitmap of
-// which tiles selected which blocks
+// scratch: a 1 KiB record per 128-row group (main lse2 per row, index normaliser per token),
+// then the bitmap of which tiles selected which blocks
 size_t index_kl_tc_workspace_bytes(const Dims& p);
 cudaError_t launch_index_kl_tc(const Dims& p, const void* q, const void* k, const float* lse,
                                const void* idx_q, const void* idx_k, const int32_t* sel,

@@ -13,14 +13,16 @@
 // Two kernels, each accumulating in TMEM so that no partial product goes through HBM:
 // * dQ (query-outer, one CTA per 128 (token, head) rows of a tile, as in the forward): per
 //   selected block S = Q K^T and dP = dO V^T into TMEM, the softmax warps form dS (bf16, in
-//   TMEM) and dQ += dS K accumulates in TMEM.  It also writes D for the second kernel.
+//   TMEM) and dQ += dS K accumulates in TMEM.  It also writes each 128-row group's lse2 and
+//   D, in row order, as one 1 KiB record for the second kernel.
 // * dK, dV (key-outer, one CTA per (sequence, KV head, key block, range of query tiles)):
 //   the tiles that selected the block are read from a bitmap built first; for every 128-row
 //   group of those tiles S^T = K Q^T and dP^T = V dO^T go to TMEM (keys on the TMEM lanes),
 //   the elementwise warps form P^T and dS^T there, and dV += P^T dO, dK += dS^T Q accumulate
 //   in TMEM over all of the CTA's groups.  A CTA adds its dK / dV to the fp32 outputs with
 //   vector atomics (a heavily selected block is split over several CTAs).
-// Every wait is bounded.
+// Warps: 8 elementwise warps (two per TMEM lane quadrant, each taking half of the columns of
+// S / dP or S^T / dP^T), a TMA producer and an MMA issuer.  Every wait is bounded.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sparse_backward_tc.cuh"
@@ -37,8 +39,9 @@ constexpr int kRows = 128;                              // rows of one Q group
 constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;       // [2 chunks][128 rows][128 B] = 32 KiB
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 192;                           // 4 math warps, producer, MMA issuer
-constexpr int kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kThreads = 320;                           // 8 math warps, producer, MMA issuer
+constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kMathWarps = 8;                           // two per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);   // both operands K-major
 constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);   // B MN-major
@@ -68,15 +71,22 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_smem, uint32_
 }
 
 // D[tmem] (+)= A[tmem, 128 x 128 bf16] B[smem, MN-major 128 x 128], the reduction over the
-// 128 rows of B: dQ += dS K, dV += P^T dO, dK += dS^T Q.
+// 128 rows of B: dQ += dS K, dV += P^T dO, dK += dS^T Q.  A's second half (K 64..127) sits at
+// columns 96..127 of its region when split (see p_col), else right after the first.
 __device__ __forceinline__ void mma_tmn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
-                                        bool accumulate) {
+                                        bool accumulate, bool split = false) {
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)
-    ptx::umma_bf16_ts(d_tmem, a_tmem + kk * 8,
+    ptx::umma_bf16_ts(d_tmem, a_tmem + kk * 8 + (split && kk >= 4 ? 64 : 0),
                       ptx::smem_desc_mn_sw128(b_smem + kk * 16 * kRowBytes, kRows * kRowBytes, 1024),
                       kIdescMN, (accumulate || kk > 0) ? 1u : 0u);
 }
+
+// Column of bf16 chunk c (32 values packed into 16 columns) written over an fp32 region of
+// 128 columns: chunks 0-1 over the region's columns 0-31, chunks 2-3 over 96-127, so each of
+// the two warps of a lane quadrant (columns 0-63 / 64-127) overwrites only columns it has
+// itself loaded.
+__device__ __forceinline__ int p_col(int c) { return c < 2 ? c * 16 : 96 + (c - 2) * 16; }
 
 __device__ __forceinline__ void raise_abort(int* abort_flag, int* status, int code) {
   *abort_flag = 1;
@@ -122,7 +132,8 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_v,
                       const int32_t* __restrict__ sel, const __nv_bfloat16* __restrict__ out,
                       const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                      float* __restrict__ dq, float* __restrict__ dvec, Dims p, int* status) {
+                      float* __restrict__ dq, float* __restrict__ rowstat, Dims p,
+                      int* status) {
   extern __shared__ uint8_t smem_raw[];
   SmemQ& s = *reinterpret_cast<SmemQ*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                        ~uintptr_t(1023));
@@ -141,8 +152,8 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_init(&s.kv_empty[i], 1);
     }
     ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.s_free, 4);
-    ptx::mbar_init(&s.ds_full, 4);
+    ptx::mbar_init(&s.s_free, kMathWarps);
+    ptx::mbar_init(&s.ds_full, kMathWarps);
     ptx::mbar_init(&s.dq_done, 1);
     ptx::mbar_init(&s.drain, 1);
     s.abort = 0;
@@ -254,15 +265,17 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_wait_timed(&s.drain, 0);
     }
   } else {
-    // --------------------------------------------------- math warps 0-3: one row each
-    const int r = warp * 32 + lane;
+    // ------------------------- math warps 0-7: warp w takes row quadrant w % 4 and the key
+    // columns (and dQ columns) 64 (w / 4) .. +63
+    const int quad = warp & 3, half = warp >> 2;
+    const int r = quad * 32 + lane;
     const int R = part * kRows + r;                      // row within the tile's Qt*G rows
     const int t = m * kQt + R / G;
     const int h = g * G + R % G;
     const bool valid = t < p.Sq;
     const float c1 = p.sm_scale * kLog2e;
     const size_t row_off = (((size_t)b * p.Sq + (valid ? t : 0)) * p.Hq + h) * kD;
-    // D = dout . out of this row, also kept for the dK / dV kernel
+    // D = dout . out of this row (both warps of the quadrant need it)
     float dsum = 0.f;
     if (valid) {
       const uint4* o4 = reinterpret_cast<const uint4*>(out + row_off);
@@ -278,10 +291,15 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           dsum = fmaf(fa.x, fc.x, fmaf(fa.y, fc.y, dsum));
         }
       }
-      dvec[((size_t)b * p.Hq + h) * p.Sq + t] = dsum;
     }
     const float lse2 = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    if (half == 0) {
+      // the group's record for the dK/dV pass: lse2 of its 128 rows, then their D
+      float* rec = rowstat + (((size_t)bg * p.nR + m) * gridDim.x + part) * 2 * kRows;
+      rec[r] = lse2;
+      rec[kRows + r] = dsum;
+    }
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     bool ok = true;
     for (int j = 0; j < n_sel; ++j) {
       const int blk = s.blocks[j];
@@ -290,28 +308,30 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       const int lim = t - blk * kBk;                       // visible columns: c <= lim
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dv[32];
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
-        ptx::tmem_ld_x32(tmem + lane_off + kColDP + c * 32, dv);
-        ptx::tmem_ld_wait();
-        if (c == 3) {
-          // every S / dP column of this block is in registers: the next block may overwrite
-          ptx::tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&s.s_free);
-        }
+      uint32_t sv[2][32], dv[2][32];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (2 * half + u) * 32, dv[u]);
+      }
+      ptx::tmem_ld_wait();
+      // this warp's S / dP columns are in registers: the next block may overwrite them
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.s_free);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = 2 * half + u;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float ds2[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const float pr = c * 32 + e + u <= lim
-                                 ? ex2(fmaf(__uint_as_float(sv[e + u]), c1, -lse2))
+          for (int w = 0; w < 2; ++w) {
+            const float pr = c * 32 + e + w <= lim
+                                 ? ex2(fmaf(__uint_as_float(sv[u][e + w]), c1, -lse2))
                                  : 0.f;
-            ds2[u] = pr * (__uint_as_float(dv[e + u]) - dsum);
+            ds2[w] = pr * (__uint_as_float(dv[u][e + w]) - dsum);
           }
           pk[e >> 1] = pack_bf16x2(ds2[0], ds2[1]);
         }
@@ -326,11 +346,13 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool have = ok && n_sel > 0 && ptx::mbar_wait(&s.dq_done, (n_sel - 1) & 1, abort);
     if (ok && n_sel > 0 && !have && lane == 0) raise_abort(&s.abort, status, 0x504);
     if (have) ptx::tc_fence_after_sync();
-    // dq = sm_scale * dQ (zero for a row with no visible key); tcgen05.ld is warp-collective,
-    // so every lane loads (`have` is the same in the whole warp) and valid rows store
+    // dq = sm_scale * dQ (zero for a row with no visible key), this warp's 64 columns;
+    // tcgen05.ld is warp-collective, so every lane loads (`have` is the same in the whole
+    // warp) and valid rows store
     float4* dst = reinterpret_cast<float4*>(dq + row_off);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int u = 0; u < 2; ++u) {
+      const int c = 2 * half + u;
       uint32_t v[32];
       if (have) {
         ptx::tmem_ld_x32(tmem + lane_off + kColDQ + c * 32, v);
@@ -363,8 +385,7 @@ struct __align__(1024) SmemKV {
   uint8_t v[kTileBytes];
   uint8_t q[2][kTileBytes];
   uint8_t dO[2][kTileBytes];
-  float lse2[2][kRows];
-  float dd[2][kRows];
+  float rec[2][2 * kRows];       // a group's lse2 [0,128) and D [128,256), per stage
   uint64_t kv_full, g_full[2], g_empty[2];
   uint64_t s_full, p_full, acc_done, drain;
   int tiles[kMaxTilesPerCta];
@@ -378,8 +399,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_do,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
-                        const uint32_t* __restrict__ bits, const float* __restrict__ lse,
-                        const float* __restrict__ dvec, float* __restrict__ dk,
+                        const uint32_t* __restrict__ bits, const float* __restrict__ rowstat,
+                        float* __restrict__ dk,
                         float* __restrict__ dv, Dims p, int words, int words_per_cta,
                         int* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -426,7 +447,7 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_init(&s.g_empty[i], 1);
     }
     ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.p_full, 4);
+    ptx::mbar_init(&s.p_full, kMathWarps);
     ptx::mbar_init(&s.acc_done, 1);
     ptx::mbar_init(&s.drain, 1);
     s.abort = 0;
@@ -459,19 +480,12 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int st = gi & 1;
       if (!ptx::mbar_wait(&s.g_empty[st], ((gi >> 1) & 1) ^ 1, abort)) { ok = false; break; }
       const int m = s.tiles[gi / parts], part = gi % parts;
-      // per-row lse (log2 units) and D of the group, +inf / 0 for rows past the sequence
-#pragma unroll
-      for (int x4 = 0; x4 < kRows / 32; ++x4) {
-        const int x = x4 * 32 + lane;
-        const int R = part * kRows + x;
-        const int t = m * kQt + R / G, h = g * G + R % G;
-        const bool valid = t < p.Sq;
-        s.lse2[st][x] = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
-        s.dd[st][x] = valid ? dvec[((size_t)b * p.Hq + h) * p.Sq + t] : 0.f;
-      }
-      __syncwarp();
       if (lane == 0) {
-        ptx::mbar_arrive_expect_tx(&s.g_full[st], 2 * kTileBytes);
+        // the group's per-row lse2 and D (+inf / 0 past the sequence), written in row order
+        // by the dQ pass, and its Q and dO rows
+        ptx::mbar_arrive_expect_tx(&s.g_full[st], 2 * kTileBytes + 2 * kRows * 4);
+        ptx::bulk_load(s.rec[st], rowstat + (((size_t)bg * p.nR + m) * parts + part) * 2 * kRows,
+                       2 * kRows * 4, &s.g_full[st]);
         const int t0 = m * kQt + part * tok_per_group;
         for (int kc = 0; kc < 2; ++kc) {
           ptx::tma_load_4d(s.q[st] + kc * kRows * kRowBytes, &tm_q, &s.g_full[st], kc * 64,
@@ -509,8 +523,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ptx::mbar_wait(&s.p_full, gi & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       if (lane == 0) {
-        mma_tmn(tmem + kColDV, tmem + kColS, ptx::smem_u32(s.dO[st]), gi > 0);
-        mma_tmn(tmem + kColDK, tmem + kColDP, ptx::smem_u32(s.q[st]), gi > 0);
+        mma_tmn(tmem + kColDV, tmem + kColS, ptx::smem_u32(s.dO[st]), gi > 0, true);
+        mma_tmn(tmem + kColDK, tmem + kColDP, ptx::smem_u32(s.q[st]), gi > 0, true);
         ptx::umma_commit(&s.acc_done);
         ptx::umma_commit(&s.g_empty[st]);
       }
@@ -522,9 +536,11 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_wait_timed(&s.drain, 0);
     }
   } else {
-    // --------------------------------------- math warps 0-3: one key of the block each
-    const int key = blk * kBk + warp * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ----------------- math warps 0-7: one key of the block per lane (quadrant w % 4); warp
+    // w takes the group rows (and dV / dK columns) 64 (w / 4) .. +63
+    const int quad = warp & 3, half = warp >> 2;
+    const int key = blk * kBk + quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c1 = p.sm_scale * kLog2e;
     bool ok = true;
     for (int gi = 0; gi < n_groups; ++gi) {
@@ -534,32 +550,36 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int t0 = m * kQt + part * tok_per_group;
       const int dj = key - t0;
       const int xlim = dj > 0 ? dj * G : 0;
-      // g_full: the producer's per-row lse / D of this group are visible; s_full: S^T, dP^T
+      // g_full: the group's per-row lse2 / D have landed; s_full: S^T, dP^T
       if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
           !ptx::mbar_wait(&s.s_full, gi & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dpv[32];
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
-        ptx::tmem_ld_x32(tmem + lane_off + kColDP + c * 32, dpv);
-        ptx::tmem_ld_wait();
+      uint32_t sv[2][32], dpv[2][32];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (2 * half + u) * 32, dpv[u]);
+      }
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = 2 * half + u;
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           float pr[2], dsv[2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int x = c * 32 + e + u;
-            pr[u] = x >= xlim ? ex2(fmaf(__uint_as_float(sv[e + u]), c1, -s.lse2[st][x])) : 0.f;
-            dsv[u] = pr[u] * (__uint_as_float(dpv[e + u]) - s.dd[st][x]);
+          for (int w = 0; w < 2; ++w) {
+            const int x = c * 32 + e + w;
+            pr[w] = x >= xlim ? ex2(fmaf(__uint_as_float(sv[u][e + w]), c1, -s.rec[st][x])) : 0.f;
+            dsv[w] = pr[w] * (__uint_as_float(dpv[u][e + w]) - s.rec[st][kRows + x]);
           }
           pp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
           dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        // P^T chunk c lands on S^T columns 16c .. 16c+15, already loaded (same for dS^T)
-        ptx::tmem_st_x16(tmem + lane_off + kColS + c * 16, pp);
-        ptx::tmem_st_x16(tmem + lane_off + kColDP + c * 16, dd);
+        // P^T / dS^T over columns this warp loaded (p_col)
+        ptx::tmem_st_x16(tmem + lane_off + kColS + p_col(c), pp);
+        ptx::tmem_st_x16(tmem + lane_off + kColDP + p_col(c), dd);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
@@ -575,7 +595,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       float4* dvr = reinterpret_cast<float4*>(dv + ((size_t)bg * p.Sk + (in_range ? key : 0)) * kD);
       float4* dkr = reinterpret_cast<float4*>(dk + ((size_t)bg * p.Sk + (in_range ? key : 0)) * kD);
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int u = 0; u < 2; ++u) {
+        const int c = 2 * half + u;
         uint32_t a[32], bk[32];
         ptx::tmem_ld_x32(tmem + lane_off + kColDV + c * 32, a);
         ptx::tmem_ld_x32(tmem + lane_off + kColDK + c * 32, bk);
@@ -633,19 +654,20 @@ bool sparse_backward_tc_supported(const Dims& p) {
 }
 
 size_t sparse_backward_tc_workspace_bytes(const Dims& p) {
-  const size_t dvec = (size_t)p.B * p.Hq * p.Sq * sizeof(float);
+  // per 128-row group: lse2 and D of its rows (1 KiB), then the bitmap
+  const size_t rowstat = (size_t)p.B * p.Hkv * p.nR * (p.Qt * p.G / kRows) * 2 * kRows * 4;
   const size_t words = (size_t)(p.nR + 31) / 32;
   const size_t bitmap = (size_t)p.B * p.Hkv * p.nB * words * sizeof(uint32_t);
-  return (dvec + 255) / 256 * 256 + bitmap;
+  return rowstat + bitmap;
 }
 
 cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* k,
                                       const void* v, const int32_t* sel, const void* out,
                                       const float* lse, const void* dout, float* dq, float* dk,
                                       float* dv, void* workspace, cudaStream_t st, int* status) {
-  const size_t dvec_bytes = ((size_t)p.B * p.Hq * p.Sq * sizeof(float) + 255) / 256 * 256;
-  float* dvec = reinterpret_cast<float*>(workspace);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + dvec_bytes);
+  const size_t rowstat_bytes = (size_t)p.B * p.Hkv * p.nR * (p.Qt * p.G / kRows) * 2 * kRows * 4;
+  float* rowstat = reinterpret_cast<float*>(workspace);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(workspace) + rowstat_bytes);
   const int words = (p.nR + 31) / 32;
   const size_t kv_bytes = (size_t)p.B * p.Hkv * p.Sk * kD * sizeof(float);
   cudaError_t e = cudaMemsetAsync(dk, 0, kv_bytes, st);
@@ -677,7 +699,7 @@ cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* 
     dim3 grid(p.Qt * p.G / kRows, p.nR, p.B * p.Hkv);
     backward_dq_tc_kernel<<<grid, kThreads, smem, st>>>(
         tq, tdo, tk, tv, sel, (const __nv_bfloat16*)out, (const __nv_bfloat16*)dout, lse, dq,
-        dvec, p, status);
+        rowstat, p, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
@@ -687,7 +709,7 @@ cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* 
     if (e != cudaSuccess) return e;
     const int wpc = tiles_per_cta(p) / 32;
     dim3 grid((words + wpc - 1) / wpc, p.nB, p.B * p.Hkv);
-    backward_dkdv_tc_kernel<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, bits, lse, dvec, dk,
+    backward_dkdv_tc_kernel<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, bits, rowstat, dk,
                                                           dv, p, words, wpc, status);
     e = cudaGetLastError();
   }

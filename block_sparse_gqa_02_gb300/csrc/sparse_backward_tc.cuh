@@ -5,7 +5,8 @@
 
 namespace msa {
 bool sparse_backward_tc_supported(const Dims& p);
-// scratch: D = dout . out per row [B, Hq, Sq] fp32, then the tile-selects-block bitmap
+// scratch: a 1 KiB record per 128-row group (lse2 and D = dout . out of its rows), then the
+// tile-selects-block bitmap
 size_t sparse_backward_tc_workspace_bytes(const Dims& p);
 cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* k,
                                       const void* v, const int32_t* sel, const void* out,
