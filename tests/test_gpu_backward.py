@@ -23,6 +23,7 @@ CASES = {
     "bf16_g4_k1": CONFIGS["p32k"].with_(seq=1200, n_heads_q=16, top_k=1, n_plants=0),
     "bf16_g2_ragged": CONFIGS["p32k"].with_(seq=700, n_heads_q=8, top_k=3, n_plants=0),
     "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=0),
+    "bf16_b2_ragged": CONFIGS["p32k"].with_(batch=2, seq=1100, top_k=4, n_plants=0),
 }
 
 
@@ -33,12 +34,12 @@ def test_sparse_prefill_backward(name):
     shape = _lib.shape_from_config(cfg)
     cur = np.array([min(cfg.seq - 1, m * cfg.q_tile + cfg.q_tile - 1) // cfg.block_size
                     for m in range(shape.n_rows)])
-    sel_np = random_selection(np.broadcast_to(cur + 1, (1, 4, shape.n_rows)), cfg.top_k, 5)
+    sel_np = random_selection(np.broadcast_to(cur + 1, (cfg.batch, 4, shape.n_rows)), cfg.top_k, 5)
     sel = torch.from_numpy(sel_np).cuda()
     gen = torch.Generator(device="cuda").manual_seed(99)
     dout = torch.randn(x["q"].shape, generator=gen, device="cuda").to(x["q"].dtype)
     out = torch.empty_like(x["q"])
-    lse = torch.empty((1, cfg.n_heads_q, cfg.seq), device="cuda")
+    lse = torch.empty((cfg.batch, cfg.n_heads_q, cfg.seq), device="cuda")
     _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
     dq = torch.full(x["q"].shape, float("nan"), device="cuda")
     dk = torch.full(x["k"].shape, float("nan"), device="cuda")
@@ -68,6 +69,7 @@ KL_CASES = {
     "bf16_g2_ragged": CONFIGS["p32k"].with_(seq=700, n_heads_q=8, top_k=3, n_plants=0),
     "bf16_g32_ragged": CONFIGS["p32k"].with_(seq=900, n_heads_q=128, top_k=3, n_plants=0),
     "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=4),
+    "bf16_b2_ragged": CONFIGS["p32k"].with_(batch=2, seq=1100, top_k=4, n_plants=2),
 }
 
 
@@ -78,10 +80,10 @@ def test_index_kl_loss(name):
     shape = _lib.shape_from_config(cfg)
     cur = np.array([min(cfg.seq - 1, m * cfg.q_tile + cfg.q_tile - 1) // cfg.block_size
                     for m in range(shape.n_rows)])
-    sel_np = random_selection(np.broadcast_to(cur + 1, (1, 4, shape.n_rows)), cfg.top_k, 6)
+    sel_np = random_selection(np.broadcast_to(cur + 1, (cfg.batch, 4, shape.n_rows)), cfg.top_k, 6)
     sel = torch.from_numpy(sel_np).cuda()
     out = torch.empty_like(x["q"])
-    lse = torch.empty((1, cfg.n_heads_q, cfg.seq), device="cuda")
+    lse = torch.empty((cfg.batch, cfg.n_heads_q, cfg.seq), device="cuda")
     _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
     loss = torch.full((1,), float("nan"), device="cuda")
     diq = torch.full(x["idx_q"].shape, float("nan"), device="cuda")

@@ -17,6 +17,7 @@ CASES = {
     "k1": CONFIGS["p32k"].with_(seq=3000, top_k=1, n_plants=2),
     "k256": CONFIGS["p32k"].with_(seq=40000, top_k=256, n_plants=8),
     "p128k": CONFIGS["p128k"],
+    "batch2_ragged": CONFIGS["p32k"].with_(batch=2, seq=2500, top_k=6, n_plants=3),
 }
 
 

@@ -140,6 +140,7 @@ INDEX_CASES = {
     "bf16_ragged_1000": lambda: small_cfg("p32k", seq=1000, n_plants=3),
     "bf16_4096_d64": lambda: small_cfg("p32k", seq=4096, index_dim=64, block_size=64),
     "bf16_8192": lambda: small_cfg("p32k", seq=8192, n_plants=5),
+    "bf16_b2_ragged": lambda: small_cfg("p32k", batch=2, seq=1300, n_plants=3),
     "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, n_plants=4),
     "decode_tiny_cache": lambda: small_cfg("d1m", batch=3, seq=77, n_plants=0),
     "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", index_dim=64,
@@ -205,6 +206,7 @@ ATTN_CASES = {
     "bf16_g4_ragged": lambda: small_cfg("p32k", seq=2000, n_heads_q=16, top_k=7),
     "bf16_g32": lambda: small_cfg("p32k", seq=1100, n_heads_q=128, top_k=3),
     "bf16_g16_k1": lambda: small_cfg("p32k", seq=700, n_heads_q=64, top_k=1),
+    "bf16_b2_ragged": lambda: small_cfg("p32k", batch=2, seq=1300, top_k=5),
     "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, top_k=8, n_plants=4),
     "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", top_k=5,
                                     head_dim=64, n_plants=2),
@@ -354,6 +356,10 @@ def test_pipeline_tiny_scaled_plants_selected():
 
 def test_pipeline_bf16_small():
     assert _pipeline(small_cfg("p32k", seq=3000, n_plants=6)) >= 0.9
+
+
+def test_pipeline_bf16_batch2():
+    assert _pipeline(small_cfg("p32k", batch=2, seq=2000, n_plants=4)) >= 0.9
 
 
 def test_pipeline_p32k_sampled():
