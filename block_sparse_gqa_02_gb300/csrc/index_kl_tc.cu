@@ -320,7 +320,11 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     ptx::tc_fence_before_sync();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&s.pass1_done);
-    // pass 2: target, loss, gz
+    // pass 2: target, loss, gz.  Of every G consecutive keys, the G rows (lanes) of a token
+    // each finish one: a reduce-scatter over the token's lanes leaves lane hh the token's
+    // target for key hh of the G, and that lane alone forms p_I, the loss term and gz for
+    // it.  Each lane writes its gz (zeros at the other keys) as its row of the d idx_q
+    // operand, so the rows of a token hold partial d idx_q that are summed at the end.
     const float lse2 = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
     if (half == 0) {
       // the group's record for the key-block pass: lse2 per row, then lseI2 per token
@@ -345,21 +349,37 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int c = 2 * half + u;
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float gz2[2];
+        for (int e0 = 0; e0 < 32; e0 += G) {
+          // this row's attention probability at keys e0 .. e0+G-1 (0 where not visible)
+          float a[G];
 #pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const bool vis = c * 32 + e + w <= lim;
-            float pt = vis ? ex2(fmaf(__uint_as_float(sv[u][e + w]), c1, -lse2)) : 0.f;
+          for (int x = 0; x < G; ++x)
+            a[x] = c * 32 + e0 + x <= lim ? ex2(fmaf(__uint_as_float(sv[u][e0 + x]), c1, -lse2))
+                                          : 0.f;
+          // reduce-scatter over the token's G lanes: lane hh ends with key e0 + hh's sum
 #pragma unroll
-            for (int o = 1; o < G; o <<= 1) pt += __shfl_xor_sync(0xffffffffu, pt, o);
-            pt *= 1.f / G;
-            const float zl = fmaf(__uint_as_float(zv[u][e + w]), c2, -lseI2);   // log2 p_I
-            const float pi = vis ? ex2(zl) : 0.f;
-            if (hh == 0 && pt > 0.f) lsum += pt * (__log2f(pt) - zl);
-            gz2[w] = pi - pt;
+          for (int st = G / 2, n = G; st >= 1; st >>= 1, n >>= 1) {
+            const bool up = (hh & st) != 0;
+#pragma unroll
+            for (int x = 0; x < n / 2; ++x) {
+              const float keep = up ? a[x + n / 2] : a[x];
+              const float send = up ? a[x] : a[x + n / 2];
+              a[x] = keep + __shfl_xor_sync(0xffffffffu, send, st);
+            }
           }
-          pk[e >> 1] = pack_bf16x2(gz2[0], gz2[1]);
+          const float pt = a[0] * (1.f / G);
+          float z = __uint_as_float(zv[u][e0]);
+#pragma unroll
+          for (int x = 1; x < G; ++x)
+            if (hh == x) z = __uint_as_float(zv[u][e0 + x]);
+          const bool vis = c * 32 + e0 + hh <= lim;
+          const float zl = fmaf(z, c2, -lseI2);                // log2 p_I
+          const float pi = vis ? ex2(zl) : 0.f;
+          if (pt > 0.f) lsum += pt * (__log2f(pt) - zl);
+          const float gz = pi - pt;
+#pragma unroll
+          for (int x = 0; x < G; x += 2)
+            pk[(e0 + x) >> 1] = pack_bf16x2(hh == x ? gz : 0.f, hh == x + 1 ? gz : 0.f);
         }
         // gz over S columns this warp loaded (p_col)
         ptx::tmem_st_x16(tmem + lane_off + kColS + p_col(c), pk);
@@ -381,18 +401,23 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tmem_ld_x32(tmem + lane_off + kColDQ + c * 32, v);
         ptx::tmem_ld_wait();
       }
+      // the token's d idx_q: the sum of its G rows' partial sums
+      float dv[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float x = have ? __uint_as_float(v[e]) : 0.f;
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+        dv[e] = x * p.index_scale;
+      }
       if (valid && hh == 0) {
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(dst + c * 32 + e) =
-              have ? make_float4(__uint_as_float(v[e]) * p.index_scale,
-                                 __uint_as_float(v[e + 1]) * p.index_scale,
-                                 __uint_as_float(v[e + 2]) * p.index_scale,
-                                 __uint_as_float(v[e + 3]) * p.index_scale)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
+              make_float4(dv[e], dv[e + 1], dv[e + 2], dv[e + 3]);
       }
     }
-    // the loss of this warp's rows and columns (one lane per token), natural log
+    // the loss of this warp's keys (each (token, key) term on one lane), natural log
     float lv = lsum * kLn2;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
