@@ -134,3 +134,31 @@ def test_python_binding_raises(lib):
     with pytest.raises(_lib.MsaError) as ei:
         _lib.msa_index_scores(s, None, FAKE, FAKE, stream=0)
     assert ei.value.status == MSA_ERR_INVALID_ARG
+
+
+def test_training_workspace_and_checks(lib):
+    """The tensor-core backward and index KL need a workspace (sized by which = 2 / 3) and
+    refuse a missing or short one; CUDA-core shapes need none."""
+    tc = make_shape(1, 4096, 4096, 32, 4, 128, 128, 128, 16, 64, "bf16")
+    simt = make_shape(1, 1024, 1024, 16, 4, 64, 64, 64, 4, 64, "f32")
+    for which in (2, 3):
+        need = lib.msa_workspace_bytes(ctypes.byref(tc), which)
+        assert need > 0 and need % 16 == 0
+        assert lib.msa_workspace_bytes(ctypes.byref(simt), which) == 0
+        assert lib.msa_workspace_bytes(ctypes.byref(_good_decode()), which) == 0
+    need = lib.msa_workspace_bytes(ctypes.byref(tc), 2)
+    args = [FAKE] * 10
+    assert lib.msa_sparse_prefill_backward(ctypes.byref(tc), *args, None, need,
+                                           None) == MSA_ERR_INVALID_ARG
+    assert b"workspace" in lib.msa_last_error()
+    assert lib.msa_sparse_prefill_backward(ctypes.byref(tc), *args, FAKE, need - 16,
+                                           None) == MSA_ERR_INVALID_ARG
+    need = lib.msa_workspace_bytes(ctypes.byref(tc), 3)
+    args = [FAKE] * 9
+    assert lib.msa_index_kl_loss(ctypes.byref(tc), *args, FAKE, need - 16,
+                                 None) == MSA_ERR_INVALID_ARG
+    assert b"workspace" in lib.msa_last_error()
+    # decode shapes are not training shapes
+    d = _good_decode()
+    assert lib.msa_sparse_prefill_backward(ctypes.byref(d), *([FAKE] * 10), FAKE, 1 << 30,
+                                           None) == MSA_ERR_INVALID_ARG
