@@ -181,13 +181,15 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (warp == kProducerWarp) {
     int issued = 0;
     bool ok = true;
-    if (lane == 0 && n_sel > 0) {
+    // test hook: issue nothing, so the consumers' bounded waits run out
+    const int n_load = p.inject == 1 ? 0 : n_sel;
+    if (lane == 0 && n_load > 0) {
       ptx::mbar_arrive_expect_tx(&s.q_full, kTileBytes);
       for (int kc = 0; kc < 2; ++kc)
         ptx::tma_load_4d(s.q + kc * kRows * kRowBytes, &tm_q, &s.q_full, kc * 64, g * G, t0, b);
     }
     // the block ring: pass 1 loads idx_k blocks, pass 2 idx_k and K blocks
-    for (int rr = 0; rr < 2 * n_sel; ++rr) {
+    for (int rr = 0; rr < 2 * n_load; ++rr) {
       const int st = rr & 1;
       if (!ptx::mbar_wait(&s.ring_empty[st], ((rr >> 1) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
@@ -206,7 +208,7 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x701);
-    if (*abort && lane == 0 && n_sel > 0) {
+    if (*abort && lane == 0 && n_load > 0) {
       ptx::mbar_wait_timed(&s.q_full, 0);
       for (int rr = issued > 2 ? issued - 2 : 0; rr < issued; ++rr)
         ptx::mbar_wait_timed(&s.ring_full[rr & 1], (rr >> 1) & 1);

@@ -189,7 +189,9 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ------------------------------------------------------------- TMA producer
     int issued = 0;
     bool ok = true;
-    if (lane == 0 && n_sel > 0) {
+    // test hook: issue nothing, so the consumers' bounded waits run out
+    const int n_load = p.inject == 1 ? 0 : n_sel;
+    if (lane == 0 && n_load > 0) {
       ptx::mbar_arrive_expect_tx(&s.qd_full, 2 * kTileBytes);
       const int t0 = m * kQt + part * tok_per_group;
       for (int kc = 0; kc < 2; ++kc) {
@@ -198,7 +200,7 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                          b);
       }
     }
-    for (int j = 0; j < n_sel; ++j) {
+    for (int j = 0; j < n_load; ++j) {
       const int st = j & 1;
       if (!ptx::mbar_wait(&s.kv_empty[st], ((j >> 1) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
@@ -215,7 +217,7 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x501);
-    if (*abort && lane == 0 && n_sel > 0) {
+    if (*abort && lane == 0 && n_load > 0) {
       ptx::mbar_wait_timed(&s.qd_full, 0);
       for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
         ptx::mbar_wait_timed(&s.kv_full[j & 1], (j >> 1) & 1);
