@@ -81,6 +81,13 @@ msa_status make_dims(const msa_shape* s, Dims* d) {
   const long long nB = ((long long)s->seq_k + s->block_size - 1) / s->block_size;
   if (nB > kMaxBlocks)
     return fail(MSA_ERR_UNSUPPORTED, "%lld blocks per sequence: at most %d", nB, kMaxBlocks);
+  // query tiles and (sequence, KV head) pairs index grid dimensions of at most 65535
+  const long long nR = ((long long)s->seq_q + s->q_tile - 1) / s->q_tile;
+  if (nR > 65535)
+    return fail(MSA_ERR_UNSUPPORTED, "%lld query tiles per sequence: at most 65535", nR);
+  if ((long long)s->batch * s->n_heads_kv > 65535)
+    return fail(MSA_ERR_UNSUPPORTED, "batch * n_heads_kv = %lld: at most 65535",
+                (long long)s->batch * s->n_heads_kv);
   d->B = s->batch;
   d->Sq = s->seq_q;
   d->Sk = s->seq_k;

@@ -76,12 +76,13 @@ typedef struct msa_shape {
   int32_t seq_q;       /* prefill: T; decode: 1 */
   int32_t seq_k;       /* prefill: T; decode: cache length L >= 1 */
   int32_t n_heads_q;   /* Hq, a multiple of n_heads_kv */
-  int32_t n_heads_kv;  /* Hkv = number of index query heads */
+  int32_t n_heads_kv;  /* Hkv = number of index query heads; batch * Hkv <= 65535 */
   int32_t head_dim;    /* d: 64 or 128 */
   int32_t index_dim;   /* dI: 64 or 128 */
-  int32_t block_size;  /* keys per block, >= 1 */
+  int32_t block_size;  /* keys per block, >= 1; at most 32768 blocks per sequence */
   int32_t top_k;       /* blocks per KV head, current block included, >= 1 */
-  int32_t q_tile;      /* queries sharing one selection: prefill divides block_size; decode 1 */
+  int32_t q_tile;      /* queries sharing one selection: prefill divides block_size (at most
+                        * 65535 tiles per sequence); decode 1 */
   int32_t dtype;       /* msa_dtype of q, k, v, idx_q, idx_k, out */
   float sm_scale;      /* softmax scale; 0 means 1/sqrt(head_dim) */
   float index_scale;   /* index logit scale; 0 means 1/sqrt(index_dim) */

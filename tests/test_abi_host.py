@@ -83,6 +83,16 @@ def test_too_many_blocks(lib):
     assert call_index(lib, s) == MSA_ERR_UNSUPPORTED
 
 
+def test_grid_limits(lib):
+    # 65536 query tiles (q_tile 1), and batch * n_heads_kv beyond a grid dimension
+    s = make_shape(1, 65536, 65536, 16, 4, 64, 64, 64, 4, 1, "bf16")
+    assert call_index(lib, s) == MSA_ERR_UNSUPPORTED
+    assert b"query tiles" in lib.msa_last_error()
+    s = make_shape(16384, 1024, 1024, 32, 8, 64, 64, 64, 4, 64, "bf16")
+    assert call_index(lib, s) == MSA_ERR_UNSUPPORTED
+    assert b"n_heads_kv" in lib.msa_last_error()
+
+
 def test_null_and_misaligned_pointers(lib):
     s = _good_prefill()
     assert call_index(lib, s, a=None) == MSA_ERR_INVALID_ARG
