@@ -408,7 +408,19 @@ def block_topk_shared_prefill(scores, seq_len, q_tile, block_size, top_k):
 # Training: gradients of the sparse attention (the main branch's backward pass)
 # ---------------------------------------------------------------------------
 
-def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=None):
+def _sample_masks(m, J, block_size, tiles, key_blocks):
+    """For a sampled evaluation: whether query tile m's rows are wanted, and which of its
+    keys J lie in the wanted key blocks (None: all outputs wanted)."""
+    if tiles is None and key_blocks is None:
+        return True, np.ones(J.shape, dtype=bool)
+    rows = tiles is not None and m in tiles
+    keys = (np.isin(J // block_size, key_blocks) if key_blocks is not None
+            else np.zeros(J.shape, dtype=bool))
+    return rows, keys
+
+
+def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=None,
+                              tiles=None, key_blocks=None):
     """Gradients of L = sum(dout * out) for out = sparse_attention(q, k, v, sel, ...) (prefill).
 
     With z_j = sm_scale q.k_j over the row's keys J (selected blocks, j <= t),
@@ -416,13 +428,17 @@ def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=N
       dv_j += p_j dout,   dp_j = dout . v_j,   ds_j = p_j (dp_j - D),
       dq    = sm_scale sum_j ds_j k_j,        dk_j += sm_scale ds_j q.
     A key block selected by several tiles collects the contributions of all of them.
-    Returns (dq [B,T,Hq,d], dk [B,Hkv,T,d], dv [B,Hkv,T,d]) in float64.
+    Returns (dq [B,T,Hq,d], dk [B,Hkv,T,d], dv [B,Hkv,T,d]) in float64.  Given `tiles` and /
+    or `key_blocks`, only dq of those query tiles and dk, dv of those key blocks are formed
+    (every tile that selected a wanted block still contributes); the rest stays zero.
     """
     B, T, Hq, d = q.shape
     Hkv = k.shape[1]
     G = Hq // Hkv
     if sm_scale is None or sm_scale == 0:
         sm_scale = default_scale(d)
+    tiles = None if tiles is None else set(int(x) for x in tiles)
+    key_blocks = None if key_blocks is None else np.asarray(list(key_blocks))
     dq = np.zeros((B, T, Hq, d))
     dk = np.zeros((B, Hkv, T, d))
     dv = np.zeros((B, Hkv, T, d))
@@ -433,6 +449,9 @@ def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=N
             for g in range(Hkv):
                 J = selected_keys(sel[b, g, m], block_size, T)
                 if J.size == 0:
+                    continue
+                want_rows, want_keys = _sample_masks(m, J, block_size, tiles, key_blocks)
+                if not want_rows and not want_keys.any():
                     continue
                 hs = slice(g * G, (g + 1) * G)
                 qr = _rows(q, b, slice(int(t_idx[0]), int(t_idx[-1]) + 1), hs)     # [n, G, d]
@@ -449,9 +468,11 @@ def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=N
                 D = (dor * o).sum(axis=2, keepdims=True)                           # [n, G, 1]
                 dp = np.matmul(dor, vj.T)                                          # [n, G, |J|]
                 ds = p * (dp - D)
-                dq[b, t_idx, hs] += sm_scale * np.matmul(ds, kj)
-                dk[b, g, J] += sm_scale * np.einsum("ngj,ngc->jc", ds, qr)
-                dv[b, g, J] += np.einsum("ngj,ngc->jc", p, dor)
+                if want_rows:
+                    dq[b, t_idx, hs] += sm_scale * np.matmul(ds, kj)
+                Jw = J[want_keys]
+                dk[b, g, Jw] += sm_scale * np.einsum("ngj,ngc->jc", ds[:, :, want_keys], qr)
+                dv[b, g, Jw] += np.einsum("ngj,ngc->jc", p[:, :, want_keys], dor)
     return dq, dk, dv
 
 
@@ -460,7 +481,7 @@ def sparse_attention_backward(q, k, v, sel, dout, block_size, q_tile, sm_scale=N
 # ---------------------------------------------------------------------------
 
 def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
-                  index_scale=None):
+                  index_scale=None, tiles=None, key_blocks=None):
     """KL loss that trains the index branch toward the main branch's attention ("Sparse
     Attention Cannot Be Directly Ported Across Architectures", paragraph introducing MSA;
     aietalks.com, "MSA uses a lightweight index branch before sparse attention": the index
@@ -471,7 +492,9 @@ def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
     distribution averaged over the group's G query heads, held constant; the index
     distribution is the softmax over J of the index logits index_scale <idx_q[t,g], idx_k[j]>;
     the loss is sum over (t, g) of KL(target || index).  Returns (loss, d idx_q, d idx_k) in
-    float64, the gradients being those of the summed loss.
+    float64, the gradients being those of the summed loss.  Given `tiles` and / or
+    `key_blocks`, only the loss and d idx_q of those query tiles and d idx_k of those key
+    blocks are formed; the rest stays zero.
     """
     B, T, Hq, d = q.shape
     Hkv = k.shape[1]
@@ -481,6 +504,8 @@ def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
         sm_scale = default_scale(d)
     if index_scale is None or index_scale == 0:
         index_scale = default_scale(dI)
+    tiles = None if tiles is None else set(int(x) for x in tiles)
+    key_blocks = None if key_blocks is None else np.asarray(list(key_blocks))
     loss = 0.0
     diq = np.zeros((B, T, Hkv, dI))
     dik = np.zeros((B, T, dI))
@@ -492,6 +517,9 @@ def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
             for g in range(Hkv):
                 J = selected_keys(sel[b, g, m], block_size, T)
                 if J.size == 0:
+                    continue
+                want_rows, want_keys = _sample_masks(m, J, block_size, tiles, key_blocks)
+                if not want_rows and not want_keys.any():
                     continue
                 vis = J[None, :] <= t_idx[:, None]                                 # [n, |J|]
                 # target: main attention over J, averaged over the group's heads
@@ -511,8 +539,10 @@ def index_kl_loss(q, k, idx_q, idx_k, sel, block_size, q_tile, sm_scale=None,
                 pi = np.exp(log_pi)
                 with np.errstate(divide="ignore", invalid="ignore"):
                     terms = np.where(target > 0, target * (np.log(target) - log_pi), 0.0)
-                loss += float(terms.sum())
                 gs = np.where(vis, pi - target, 0.0)                               # dL/ds
-                diq[b, ts, g] += index_scale * np.matmul(gs, ki)
-                dik[b, J] += index_scale * np.matmul(gs.T, qi)
+                if want_rows:
+                    loss += float(terms.sum())
+                    diq[b, ts, g] += index_scale * np.matmul(gs, ki)
+                Jw = J[want_keys]
+                dik[b, Jw] += index_scale * np.matmul(gs[:, want_keys].T, qi)
     return loss, diq, dik

@@ -7,7 +7,7 @@ import oracle
 from block_sparse_gqa_02_gb300 import _lib
 from block_sparse_gqa_02_gb300.configs import CONFIGS
 from block_sparse_gqa_02_gb300.inputs import make_inputs, random_selection
-from tests.parity import check_grad
+from tests.parity import check_grad, sample_tiles
 
 pytestmark = pytest.mark.gpu
 
@@ -105,3 +105,52 @@ def test_index_kl_loss(name):
     n_terms = cfg.batch * cfg.seq * cfg.n_heads_kv
     assert abs(loss.item() - ref_loss) <= 1e-3 * abs(ref_loss) + 1e-6 * n_terms, \
         (loss.item(), ref_loss)
+
+
+def test_training_p32k_sampled():
+    """The 32K workload the bench times, run in full on the GPU: the tensor-core backward and
+    index KL against the oracle on sampled query tiles (dq, d idx_q) and sampled key blocks
+    (dk, dv, d idx_k; late blocks, which few tiles select, so that the oracle's sampled
+    evaluation stays short), on a seeded selection of 16 blocks per (tile, KV head)."""
+    cfg = CONFIGS["p32k"]
+    x = make_inputs(cfg, device="cuda")
+    shape = _lib.shape_from_config(cfg)
+    nR, nB = shape.n_rows, shape.n_blocks
+    cur = np.array([min(cfg.seq - 1, m * cfg.q_tile + cfg.q_tile - 1) // cfg.block_size
+                    for m in range(nR)])
+    sel_np = random_selection(np.broadcast_to(cur + 1, (1, 4, nR)), cfg.top_k, 9)
+    sel = torch.from_numpy(sel_np).cuda()
+    out = torch.empty_like(x["q"])
+    lse = torch.empty((1, cfg.n_heads_q, cfg.seq), device="cuda")
+    _lib.msa_sparse_prefill(shape, x["q"], x["k"], x["v"], sel, out, lse)
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    dout = torch.randn(x["q"].shape, generator=gen, device="cuda").to(x["q"].dtype)
+    grads = [torch.empty(x[n].shape, device="cuda") for n in ("q", "k", "v")]
+    ws = torch.empty(_lib.msa_workspace_bytes(shape, 2) // 4 + 1, device="cuda")
+    _lib.msa_sparse_prefill_backward(shape, x["q"], x["k"], x["v"], sel, out, lse, dout,
+                                     *grads, ws)
+    loss = torch.empty(1, device="cuda")
+    kl_grads = [torch.empty(x[n].shape, device="cuda") for n in ("idx_q", "idx_k")]
+    ws = torch.empty(_lib.msa_workspace_bytes(shape, 3) // 4 + 1, device="cuda")
+    _lib.msa_index_kl_loss(shape, x["q"], x["k"], lse, x["idx_q"], x["idx_k"], sel, loss,
+                           *kl_grads, ws)
+    _lib.msa_get_device_status()
+    tiles = sample_tiles(nR, seed=13)
+    blocks = [nB - 1, nB - 4, nB - 56]
+    rows = torch.from_numpy(np.concatenate(
+        [np.arange(m * cfg.q_tile, (m + 1) * cfg.q_tile) for m in tiles])).cuda()
+    keys = torch.from_numpy(np.concatenate(
+        [np.arange(b * cfg.block_size, (b + 1) * cfg.block_size) for b in blocks])).cuda()
+    rq, rk, rv = oracle.sparse_attention_backward(x["q"], x["k"], x["v"], sel_np, dout,
+                                                  cfg.block_size, cfg.q_tile, tiles=tiles,
+                                                  key_blocks=blocks)
+    r_rows, r_keys = rows.cpu().numpy(), keys.cpu().numpy()
+    check_grad(grads[0].index_select(1, rows), rq[:, r_rows], "bf16", "p32k dq")
+    check_grad(grads[1].index_select(2, keys), rk[:, :, r_keys], "bf16", "p32k dk")
+    check_grad(grads[2].index_select(2, keys), rv[:, :, r_keys], "bf16", "p32k dv")
+    _, riq, rik = oracle.index_kl_loss(x["q"], x["k"], x["idx_q"], x["idx_k"], sel_np,
+                                       cfg.block_size, cfg.q_tile, tiles=tiles,
+                                       key_blocks=blocks)
+    check_grad(kl_grads[0].index_select(1, rows), riq[:, r_rows], "bf16", "p32k d idx_q")
+    check_grad(kl_grads[1].index_select(1, keys), rik[:, r_keys], "bf16", "p32k d idx_k")
+    assert np.isfinite(loss.item()) and loss.item() > 0

@@ -1,4 +1,5 @@
 """The oracle against its pins (CPU only)."""
+import numpy as np
 import pytest
 
 import oracle
@@ -35,3 +36,29 @@ def test_shared_selection_loses_head_diversity():
         return hit / tot
     assert recall(own) == 1.0
     assert recall(shared) < 0.8
+
+
+def test_sampled_training_gradients_equal_full():
+    """The oracle's sampled evaluation (chosen query tiles, chosen key blocks) returns exactly
+    the full evaluation's values there."""
+    r = np.random.default_rng(12)
+    B, T, Hq, Hkv, d, bs, qt, kk = 1, 40, 4, 2, 3, 4, 2, 3
+    q, dout = r.standard_normal((B, T, Hq, d)), r.standard_normal((B, T, Hq, d))
+    k, v = r.standard_normal((B, Hkv, T, d)), r.standard_normal((B, Hkv, T, d))
+    iq, ik = r.standard_normal((B, T, Hkv, 5)), r.standard_normal((B, T, 5))
+    nT, nB = T // qt, T // bs
+    sel = oracle.block_topk_prefill(r.standard_normal((B, Hkv, nT, nB)), T, qt, bs, kk)
+    tiles, blocks = [1, 7, 19], [0, 4, 9]
+    rows = np.concatenate([np.arange(m * qt, (m + 1) * qt) for m in tiles])
+    keys = np.concatenate([np.arange(b * bs, (b + 1) * bs) for b in blocks])
+    full = oracle.sparse_attention_backward(q, k, v, sel, dout, bs, qt)
+    part = oracle.sparse_attention_backward(q, k, v, sel, dout, bs, qt, tiles=tiles,
+                                            key_blocks=blocks)
+    assert np.array_equal(part[0][:, rows], full[0][:, rows])
+    for i in (1, 2):
+        assert np.allclose(part[i][:, :, keys], full[i][:, :, keys], rtol=1e-13, atol=1e-14)
+    lf, qf, kf = oracle.index_kl_loss(q, k, iq, ik, sel, bs, qt)
+    lp, qp, kp = oracle.index_kl_loss(q, k, iq, ik, sel, bs, qt, tiles=tiles, key_blocks=blocks)
+    assert np.array_equal(qp[:, rows], qf[:, rows])
+    assert np.allclose(kp[:, keys], kf[:, keys], rtol=1e-13, atol=1e-14)
+    assert 0 < lp < lf
