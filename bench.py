@@ -251,10 +251,10 @@ def e2e_prefill(cfg, step, stream, n_steps):
     """The same metric through the public API with host buffers.  Every step copies its own
     inputs (q, k, v, idx_q, idx_k) from pinned host memory to the device, runs the three
     library calls, and copies out and lse back to pinned host memory.  Steps are pipelined
-    the way a serving loop runs them: three streams (copy in, compute, copy out) and two
-    sets of device buffers, so step i+1's inputs and step i-1's outputs move while step i
-    computes.  The serial figure (copy in, compute, copy out, then the next step) is
-    reported alongside."""
+    the way a serving loop runs them: copy-in streams, a compute stream and copy-out
+    streams, with two sets of device buffers, so step i+1's inputs and step i-1's outputs
+    move while step i computes.  The serial figure (copy in, compute, copy out, then the
+    next step) is reported alongside."""
     names = ["q", "k", "v", "idx_q", "idx_k"]
     dev0 = step.x["q"].device
     # pinned host buffers on the memory next to this GPU: allocate them from the CPUs its
