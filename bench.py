@@ -346,6 +346,61 @@ def e2e_prefill(cfg, step, stream, n_steps):
             "serial_ms_per_step": ms_serial, "host_memory": host_note}, host
 
 
+def decode_paged(args, device, stream, flush, hbm_peak):
+    """The serving form of the decode step: the caches live in shared pools of 128-key
+    physical blocks in shuffled order, reached through a block table, with per-sequence
+    lengths.  Timed like the contiguous step (CUDA events around the three calls, L2
+    flushed before each step) for 8 sequences of 1M tokens (the same bytes as the contiguous
+    step) and for 8 sequences of mixed lengths."""
+    from block_sparse_gqa_02_gb300.inputs import make_paged_decode_inputs
+    cfg = CONFIGS["d1m"]
+    res = {"workload": "d1m in shuffled 128-key block pools (paged), batch 8"}
+    for name, lens in (("uniform_1m", [cfg.seq] * cfg.batch),
+                       ("ragged", [cfg.seq, cfg.seq // 2, cfg.seq // 4, 3 * cfg.seq // 4,
+                                   cfg.seq // 8, cfg.seq, 3 * cfg.seq // 8, 5 * cfg.seq // 8])):
+        x = make_paged_decode_inputs(cfg, lens, device=device)
+        shape = _lib.shape_from_config(cfg, batch=len(lens))
+        nb = shape.n_blocks
+        scores = torch.empty((len(lens), cfg.n_heads_kv, 1, nb), device=device)
+        sel = torch.empty((len(lens), cfg.n_heads_kv, 1, cfg.top_k), dtype=torch.int32,
+                          device=device)
+        out = torch.empty_like(x["q"])
+        lse = torch.empty((len(lens), cfg.n_heads_q, 1), device=device)
+        ws = torch.empty(_lib.msa_workspace_bytes(shape, 1) // 4 + 4, device=device)
+
+        def step():
+            _lib.msa_index_scores_paged(shape, x["seq_lens"], x["block_table"], x["n_phys"],
+                                        x["idx_q"], x["idx_k_pool"], scores, stream)
+            _lib.msa_block_topk_ragged(shape, x["seq_lens"], scores, sel, stream)
+            _lib.msa_sparse_decode_paged(shape, x["seq_lens"], x["block_table"], x["n_phys"],
+                                         x["q"], x["k_pool"], x["v_pool"], sel, out, lse, ws,
+                                         stream=stream)
+        for _ in range(args.warmup):
+            step()
+        ts = []
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            ts.append((e0, e1))
+        stream.synchronize()
+        _lib.msa_get_device_status(stream)
+        us = float(np.median([a.elapsed_time(b) for a, b in ts])) * 1e3
+        tokens = int(sum(lens))
+        # index keys streamed, plus the selected K/V blocks (k per KV head, at most the cache)
+        sel_keys = sum(min(cfg.top_k * cfg.block_size, L) for L in lens) * cfg.n_heads_kv
+        b_step = tokens * cfg.index_dim * 2 + sel_keys * 2 * cfg.head_dim * 2
+        res[name] = {"us_per_step": us, "cache_lengths": lens, "cached_tokens": tokens,
+                     "step_hbm_gbs": b_step / (us / 1e6) / 1e9,
+                     "frac_of_hbm_peak": b_step / (us / 1e6) / 1e9 / hbm_peak}
+        del x
+        torch.cuda.empty_cache()
+    return res
+
+
 def prefill_1m(args, device, stream, flush, tc_peak):
     """The same prefill pass at 1M context (a secondary measurement, same method)."""
     cfg = CONFIGS["p1m"]
@@ -583,6 +638,8 @@ def run_ours(args, rank, world, device):
         }
     if not args.no_1m and pcfg.name != "p1m":
         line["prefill_1m"] = prefill_1m(args, device, stream, flush, tc_peak)
+    if not args.no_decode and not args.no_paged and args.decode_len == 0:
+        line["decode_paged"] = decode_paged(args, device, stream, flush, hbm_peak)
     if not args.no_backward:
         line["backward_32k"] = backward_32k(args, device, stream, flush, tc_peak)
     if not args.no_e2e:
@@ -718,6 +775,8 @@ def main(argv=None):
     ap.add_argument("--no-1m", action="store_true",
                     help="skip the secondary 1M-context prefill measurement")
     ap.add_argument("--steps-1m", type=int, default=3)
+    ap.add_argument("--no-paged", action="store_true",
+                    help="skip the paged (block-table) decode measurement")
     ap.add_argument("--no-backward", action="store_true",
                     help="skip the training-path (backward) measurement")
     ap.add_argument("--no-e2e", action="store_true")
