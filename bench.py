@@ -68,18 +68,18 @@ def decode_bytes(cfg):
 # that was profiled: a changed kernel reports null until it is captured again.
 MEASURED_TRAFFIC = {
     "sparse_prefill_tc.cu": {
-        "sha256_16": "95e1cb0cc5ae2281",
+        "sha256_16": "2da88a1d91547301",
         "workload": "p128k",
         "bytes_per_launch": 4.53e9,
         "how": "dram__bytes_read.sum + dram__bytes_write.sum of one p32k launch "
-               "(336.4 + 230.0 MB), scaled by the (token, query head) rows to 128K (x8)",
+               "(336.4 + 229.9 MB), scaled by the (token, query head) rows to 128K (x8)",
     },
     "index_scan_tc.cu": {
-        "sha256_16": "f9e04bc1efc0b433",
+        "sha256_16": "86e08ca0ed2ffa41",
         "workload": "d1m",
         "bytes_per_launch": 2.18e9,
         "how": "dram__bytes_read.sum + dram__bytes_write.sum of one launch with 131072-token "
-               "caches (268.5 + 4.1 MB), scaled by the cache length to 1M (x8)",
+               "caches (268.5 + 4.0 MB), scaled by the cache length to 1M (x8)",
     },
 }
 

@@ -48,6 +48,53 @@ __device__ __forceinline__ void raise_abort(Smem& s, int* status, int code) {
   if (status) atomicExch(status, code);
 }
 
+// Which blocks a CTA scans.  Equal lengths: gridDim.x CTAs per sequence (blockIdx.y), each a
+// contiguous range of blocks_per_cta blocks.  Ragged lengths (blocks_per_cta == 0): a 1-D grid
+// whose CTAs are shared out in proportion to the sequences' block counts, every sequence
+// getting at least one, so that a short sequence does not leave its share of the SMs idle
+// while the longest one is still being read.
+struct ScanRange {
+  int b;          // sequence
+  int blk0;       // first block of the range
+  int nblk;       // blocks of the range inside the sequence
+  int rank, cnt;  // this CTA among the sequence's CTAs (they share the -inf tail)
+};
+
+__device__ ScanRange scan_range(const Dims& p, int blocks_per_cta) {
+  ScanRange r;
+  if (blocks_per_cta > 0) {
+    r.b = blockIdx.y;
+    r.blk0 = blockIdx.x * blocks_per_cta;
+    const int nB_b = (seq_len_of(p, r.b) + kBk - 1) / kBk;
+    r.nblk = max(0, min(nB_b, r.blk0 + blocks_per_cta) - r.blk0);
+    r.rank = blockIdx.x;
+    r.cnt = gridDim.x;
+    return r;
+  }
+  const int ctas = gridDim.x, c = blockIdx.x;   // ctas >= p.B, checked by the launcher
+  long long total = 0;
+  for (int bb = 0; bb < p.B; ++bb) total += (seq_len_of(p, bb) + kBk - 1) / kBk;
+  total = max(total, 1ll);
+  long long prefix = 0;
+  r.b = p.B - 1; r.blk0 = 0; r.nblk = 0; r.rank = 0; r.cnt = 1;
+  for (int bb = 0; bb < p.B; ++bb) {
+    const int nb = (seq_len_of(p, bb) + kBk - 1) / kBk;
+    const int lo = bb + (int)((long long)(ctas - p.B) * prefix / total);
+    const int hi = bb + 1 + (int)((long long)(ctas - p.B) * (prefix + nb) / total);
+    if (c >= lo && c < hi) {
+      const int cnt = hi - lo, per = (nb + cnt - 1) / cnt;
+      r.b = bb;
+      r.rank = c - lo;
+      r.cnt = cnt;
+      r.blk0 = r.rank * per;
+      r.nblk = max(0, min(nb, r.blk0 + per) - r.blk0);
+      break;
+    }
+    prefix += nb;
+  }
+  return r;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 index_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __nv_bfloat16* __restrict__ iq,
                      float* __restrict__ scores, Dims p, int blocks_per_cta, int* status) {
@@ -55,16 +102,15 @@ index_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __nv_bfloat
   Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                      ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.y;
-  const int blk0 = blockIdx.x * blocks_per_cta;
+  const ScanRange rg = scan_range(p, blocks_per_cta);
+  const int b = rg.b, blk0 = rg.blk0, nblk = rg.nblk;
   const int L = seq_len_of(p, b);                       // this sequence's cache length
   const int nB_b = (L + kBk - 1) / kBk;
-  const int nblk = max(0, min(nB_b, blk0 + blocks_per_cta) - blk0);
   const volatile int* abort = &s.abort;
-  // blocks of this CTA's range past the sequence's end hold no key
-  for (int blk = max(blk0, nB_b) + threadIdx.x / kNI; blk < min(p.nB, blk0 + blocks_per_cta);
-       blk += kThreads / kNI)
-    scores[((size_t)b * kNI + threadIdx.x % kNI) * p.nB + blk] = -INFINITY;
+  // blocks past the sequence's end hold no key: the sequence's CTAs share them out
+  for (int e = rg.rank * kThreads + threadIdx.x; e < (p.nB - nB_b) * kNI;
+       e += rg.cnt * kThreads)
+    scores[((size_t)b * kNI + e % kNI) * p.nB + nB_b + e / kNI] = -INFINITY;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -218,15 +264,17 @@ cudaError_t launch_index_scan_tc(const Dims& p, const void* idx_q, const void* i
   const uint32_t kbx[3] = {64, (uint32_t)kBk, 1};
   e = make_tensor_map_bf16(&tk, idx_k, 3, kd, ks, kbx);
   if (e != cudaSuccess) return e;
-  // one CTA per SM, split evenly over the sequences
+  // one CTA per SM: split evenly over the sequences when they have one length, in
+  // proportion to their lengths (read on the device) when they may differ
+  const bool ragged = p.seq_lens != nullptr && p.B <= sms;
   const int ctas_per_seq = max(1, (sms + p.B - 1) / p.B);
-  const int blocks_per_cta = (p.nB + ctas_per_seq - 1) / ctas_per_seq;
-  const int ctas = (p.nB + blocks_per_cta - 1) / blocks_per_cta;
+  const int blocks_per_cta = ragged ? 0 : (p.nB + ctas_per_seq - 1) / ctas_per_seq;
+  const int ctas = ragged ? sms : (p.nB + blocks_per_cta - 1) / blocks_per_cta;
   const size_t smem = sizeof(Smem) + 1024;
   e = cudaFuncSetAttribute(index_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(ctas, p.B);
+  dim3 grid(ctas, ragged ? 1 : p.B);
   index_scan_tc_kernel<<<grid, kThreads, smem, st>>>(tk, (const __nv_bfloat16*)idx_q, scores, p,
                                                      blocks_per_cta, status);
   return cudaGetLastError();

@@ -191,17 +191,13 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ptx::mbar_wait(&s.k_empty[ks], ((j / kKStages) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
-        for (int kc = 0; kc < 2; ++kc)
-          ptx::tma_load_3d(s.k[ks] + kc * kBk * kRowBytes, &tm_k, &s.k_full[ks], kc * 64,
-                           blk * kBk, bg);
+        ptx::tma_load_4d(s.k[ks], &tm_k, &s.k_full[ks], 0, blk * kBk, 0, bg);
       }
       k_issued = j + 1;
       if (!ptx::mbar_wait(&s.v_empty[vs], ((j / kVStages) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
         ptx::mbar_arrive_expect_tx(&s.v_full[vs], kTileBytes);
-        for (int kc = 0; kc < 2; ++kc)
-          ptx::tma_load_3d(s.v[vs] + kc * kBk * kRowBytes, &tm_v, &s.v_full[vs], kc * 64,
-                           blk * kBk, bg);
+        ptx::tma_load_4d(s.v[vs], &tm_v, &s.v_full[vs], 0, blk * kBk, 0, bg);
       }
       v_issued = j + 1;
       __syncwarp();
@@ -261,6 +257,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (lane == 0) {
           issue_pv(0, j);
           ptx::umma_commit(&s.pv_done[0]);
+          if (!more) ptx::umma_commit(&s.o_full[0]);   // tile 0's epilogue overlaps the last P.V of tile 1
         }
         __syncwarp();
         if (more) {
@@ -279,10 +276,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           issue_pv(1, j);
           ptx::umma_commit(&s.pv_done[1]);
           ptx::umma_commit(&s.v_empty[j % kVStages]);
-          if (!more) {
-            ptx::umma_commit(&s.o_full[0]);
-            ptx::umma_commit(&s.o_full[1]);
-          }
+          if (!more) ptx::umma_commit(&s.o_full[1]);
         }
         __syncwarp();
         if (more) {
@@ -510,13 +504,16 @@ cudaError_t launch_sparse_prefill_tc(const Dims& p, const void* q, const void* k
   const uint64_t qs[3] = {(uint64_t)kD * 2, (uint64_t)p.Hq * kD * 2,
                           (uint64_t)p.Sq * p.Hq * kD * 2};
   const uint32_t qb[4] = {64, (uint32_t)p.G, (uint32_t)(kTileRows / p.G), 1};
-  // k, v [B, Hkv, Sk, d] as (d, Sk, B * Hkv); one box = 64 dims x 128 keys
-  const uint64_t kd[3] = {(uint64_t)kD, (uint64_t)p.Sk, (uint64_t)p.B * p.Hkv};
-  const uint64_t ks[2] = {(uint64_t)kD * 2, (uint64_t)p.Sk * kD * 2};
-  const uint32_t kb[3] = {64, (uint32_t)kBk, 1};
+  // k, v [B, Hkv, Sk, d] as (64 dims, Sk, 2 halves of d, B * Hkv): the half-of-d axis has the
+  // smallest stride (128 B) but sits outside the key axis, so one box {64, 128, 2, 1} lands a
+  // whole block as [half][128 keys][128 B], the two swizzled K-major chunks the UMMAs read
+  // (one copy per block instead of one per half)
+  const uint64_t kd[4] = {64, (uint64_t)p.Sk, 2, (uint64_t)p.B * p.Hkv};
+  const uint64_t ks[3] = {(uint64_t)kD * 2, 128, (uint64_t)p.Sk * kD * 2};
+  const uint32_t kb[4] = {64, (uint32_t)kBk, 2, 1};
   cudaError_t e = make_tensor_map_bf16(&tq, q, 4, qd, qs, qb);
-  if (e == cudaSuccess) e = make_tensor_map_bf16(&tk, k, 3, kd, ks, kb);
-  if (e == cudaSuccess) e = make_tensor_map_bf16(&tv, v, 3, kd, ks, kb);
+  if (e == cudaSuccess) e = make_tensor_map_bf16(&tk, k, 4, kd, ks, kb);
+  if (e == cudaSuccess) e = make_tensor_map_bf16(&tv, v, 4, kd, ks, kb);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(Smem) + 1024;
   e = cudaFuncSetAttribute(sparse_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
