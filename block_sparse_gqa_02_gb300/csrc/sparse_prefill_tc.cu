@@ -13,8 +13,9 @@
 // written over the first 64 columns of S and read by the P.V MMA straight from TMEM.
 // Warps: 0-3 softmax + epilogue of Q tile 0, 4-7 of Q tile 1, 8 TMA producer, 9 MMA issuer.
 // Online softmax in the log2 domain with conditional rescaling: the running max used for
-// the exponent only moves when a block raises the row max by more than 8 (a factor 256),
-// so the O accumulator is rarely rescaled.  Every wait is bounded.
+// the exponent only moves when a block would push the row's P past a bound (its sum past
+// 2^9 in a later block; its maximum past 2^8 in a row's first or diagonal block), so the O
+// accumulator is rarely rescaled.  Every wait is bounded.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sparse_prefill_tc.cuh"
@@ -39,7 +40,8 @@ constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, kBk, 0, 0);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, kD, 0, 1);
-constexpr float kRescaleThreshold = 8.0f;   // log2 units
+constexpr float kRescaleThreshold = 8.0f;   // log2 units, on a block's maximum
+constexpr float kSumThreshold = 512.0f;     // on a block's P sum (bounds every P by 2^9)
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct __align__(1024) Smem {
@@ -360,10 +362,10 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (__all_sync(0xffffffffu, m_used != -INFINITY && lim >= kBk - 1)) {
         // A later block with no masked key: P is formed with the running base while S
         // streams in from TMEM a chunk at a time (the next chunk loads while this one is
-        // exponentiated), and the block's maximum is checked afterwards.  P chunk c lands on
-        // S columns 16c .. 16c+15, which were loaded before.
+        // exponentiated), and the block's P sum is checked afterwards (no per-column maximum
+        // is taken: a sum within the bound bounds every P).  P chunk c lands on S columns
+        // 16c .. 16c+15, which were loaded before.
         const uint64_t negm = f32x2(-m_used, -m_used);
-        float mc[4];
         uint64_t acc[4];
         ptx::tmem_ld_x32(s_addr, sv[0]);
         ptx::tmem_ld_wait();
@@ -371,12 +373,10 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < 4; ++c) {
           if (c < 3) ptx::tmem_ld_x32(s_addr + (c + 1) * 32, sv[c + 1]);
           uint32_t pk[16];
-          mc[c] = -INFINITY;
           acc[c] = f32x2(0.f, 0.f);
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float x0 = __uint_as_float(sv[c][e]), x1 = __uint_as_float(sv[c][e + 1]);
-            mc[c] = max3(mc[c], x0, x1);
             const uint64_t y = fma_f32x2(f32x2(x0, x1), c1x2, negm);
             const float p0 = ex2(lo_f32(y)), p1 = ex2(hi_f32(y));
             acc[c] = add_f32x2(acc[c], f32x2(p0, p1));
@@ -385,21 +385,29 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           ptx::tmem_st_x16(s_addr + c * 16, pk);
           if (c < 3) ptx::tmem_ld_wait();
         }
-        const float mb = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3])) * c1;
-        const bool redo = mb > m_used + kRescaleThreshold;
-        float alpha = 1.f;
-        if (redo) {
-          alpha = ex2(m_used - mb);
-          m_used = mb;
-        }
+        // the block's P sum bounds every P of the row: at most 2^9 keeps them all small
+        const uint64_t accs = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
+        const float lb = lo_f32(accs) + hi_f32(accs);
+        const bool redo = !(lb <= kSumThreshold);
         if (__any_sync(0xffffffffu, redo)) {
-          // rare: some row's maximum passed its base by more than the threshold; the warp
-          // redoes the block (rows that keep their base recompute the same P)
+          // rare: a row's P grew past the bound; the warp redoes the block from the block
+          // maximum (rows that keep their base recompute the same P)
+          float alpha = 1.f;
+          if (redo) {
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                mx[c] = max3(mx[c], __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+            const float mb = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c1;
+            alpha = ex2(m_used - mb);
+            m_used = mb;
+          }
           l = l * alpha + p_from_sv(m_used);
           rescale_o(alpha);
         } else {
-          const uint64_t accs = add_f32x2(add_f32x2(acc[0], acc[1]), add_f32x2(acc[2], acc[3]));
-          l += lo_f32(accs) + hi_f32(accs);
+          l += lb;
         }
       } else {
         // a row's first block, or a block with masked keys: the block maximum first
