@@ -99,11 +99,29 @@ __global__ void __launch_bounds__(kThreads) block_topk_kernel(const float* __res
     return;
   }
   const int n = cb;
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    float x = srow[i];
-    if (shared)
+  if (!shared) {
+    // eight loads in flight per thread before any is used (a row of 8192 candidates is
+    // eight rounds of the CTA)
+    constexpr int kBatch = 8;
+    for (int i0 = threadIdx.x; i0 < n; i0 += kThreads * kBatch) {
+      float xs[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u * kThreads;
+        xs[u] = i < n ? __ldg(srow + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u * kThreads;
+        if (i < n) keys[i] = order_key(xs[u]);
+      }
+    }
+  } else {
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      float x = srow[i];
       for (int h = 1; h < p.Hkv; ++h) x = __fadd_rn(x, srow[h * head_stride + i]);
-    keys[i] = order_key(x);
+      keys[i] = order_key(x);
+    }
   }
 
   // radix select of the want-th largest key, 8 bits at a time from the top

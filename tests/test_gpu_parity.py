@@ -226,11 +226,13 @@ def test_sparse_attention(name):
     check_lse(got_l, ref_l, cfg.dtype, name)
 
 
-@pytest.mark.parametrize("per_key", [0.75, 3.0])
+@pytest.mark.parametrize("per_key", [0.05, 0.75, 3.0])
 def test_prefill_rows_rescale_unevenly(per_key):
-    """Even heads' row maxima climb by ~94 (0.75 per key) or ~380 logits per block, far past
-    the softmax's rescale threshold, while odd heads' stay flat: rows of one warp take the
-    rescaling path and rows beside them do not."""
+    """Even heads' row maxima climb by ~6 (0.05 per key), ~94 (0.75) or ~380 logits per
+    block while odd heads' stay flat: rows of one warp take the rescaling path and rows
+    beside them do not.  At 0.05 per key a later block lifts every key of an even head a
+    little (0.8 in log2 units per block), so its P sum passes the streaming path's bound
+    long before any single P would pass 2^8; at 0.75 and 3.0 single keys pass it by far."""
     cfg = small_cfg("p32k", seq=2000, top_k=6, n_plants=0)
     x = add_score_ramp(make_inputs(cfg, device=DEV), per_key, seed=3)
     shape = _lib.shape_from_config(cfg)
