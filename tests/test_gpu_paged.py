@@ -39,6 +39,10 @@ LENS = {
     "ragged_small": [1, 127, 128, 129, 4097, 9000],
     "ragged_with_empty": [0, 5000, 1, 70001],
     "ragged_long": [1 << 18, 123457, 65536, 3],
+    # the scan shares its CTAs out by length: one long cache takes most of them
+    "one_long_many_short": [200_000] + [1 + 37 * i for i in range(19)],
+    # more sequences than SMs: the scan falls back to splitting each sequence evenly
+    "more_sequences_than_sms": [1 + (97 * i) % 700 for i in range(160)],
 }
 
 
