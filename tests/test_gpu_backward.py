@@ -24,6 +24,10 @@ CASES = {
     "bf16_g2_ragged": CONFIGS["p32k"].with_(seq=700, n_heads_q=8, top_k=3, n_plants=0),
     "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=0),
     "bf16_b2_ragged": CONFIGS["p32k"].with_(batch=2, seq=1100, top_k=4, n_plants=0),
+    # the largest groups of the tensor-core backward: 32, 64 and 128 heads per KV head
+    "bf16_g32_ragged": CONFIGS["p32k"].with_(seq=900, n_heads_q=128, top_k=3, n_plants=0),
+    "bf16_g64_ragged": CONFIGS["p32k"].with_(seq=500, n_heads_q=256, top_k=3, n_plants=0),
+    "bf16_g128_ragged": CONFIGS["p32k"].with_(seq=300, n_heads_q=512, top_k=2, n_plants=0),
 }
 
 
@@ -68,6 +72,7 @@ KL_CASES = {
     "bf16_g4_k1": CONFIGS["p32k"].with_(seq=1200, n_heads_q=16, top_k=1, n_plants=0),
     "bf16_g2_ragged": CONFIGS["p32k"].with_(seq=700, n_heads_q=8, top_k=3, n_plants=0),
     "bf16_g32_ragged": CONFIGS["p32k"].with_(seq=900, n_heads_q=128, top_k=3, n_plants=0),
+    "bf16_g64_ragged": CONFIGS["p32k"].with_(seq=500, n_heads_q=256, top_k=3, n_plants=0),
     "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=4),
     "bf16_b2_ragged": CONFIGS["p32k"].with_(batch=2, seq=1100, top_k=4, n_plants=2),
 }

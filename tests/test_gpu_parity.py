@@ -205,6 +205,10 @@ ATTN_CASES = {
     "bf16_4096_k16": lambda: small_cfg("p32k", seq=4096),
     "bf16_g4_ragged": lambda: small_cfg("p32k", seq=2000, n_heads_q=16, top_k=7),
     "bf16_g32": lambda: small_cfg("p32k", seq=1100, n_heads_q=128, top_k=3),
+    # the largest groups the tensor-core prefill takes: 64 and 128 query heads per KV head
+    # (a Q tile of 128 rows is then 2 tokens, or 1)
+    "bf16_g64": lambda: small_cfg("p32k", seq=600, n_heads_q=256, top_k=3, n_plants=0),
+    "bf16_g128": lambda: small_cfg("p32k", seq=333, n_heads_q=512, top_k=2, n_plants=0),
     "bf16_g16_k1": lambda: small_cfg("p32k", seq=700, n_heads_q=64, top_k=1),
     "bf16_b2_ragged": lambda: small_cfg("p32k", batch=2, seq=1300, top_k=5),
     "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, top_k=8, n_plants=4),
@@ -215,6 +219,9 @@ ATTN_CASES = {
                                    n_plants=4),
     "decode_g4_k3": lambda: small_cfg("d1m", batch=5, seq=1000, n_heads_q=16, top_k=3,
                                       n_plants=2),
+    # more query heads per KV head than the tensor-core decode's 16 rows
+    "decode_g32": lambda: small_cfg("d1m", batch=2, seq=3000, n_heads_q=128, top_k=6,
+                                    n_plants=2),
 }
 
 
