@@ -211,10 +211,13 @@ ATTN_CASES = {
     "bf16_g128": lambda: small_cfg("p32k", seq=333, n_heads_q=512, top_k=2, n_plants=0),
     "bf16_g16_k1": lambda: small_cfg("p32k", seq=700, n_heads_q=64, top_k=1),
     "bf16_b2_ragged": lambda: small_cfg("p32k", batch=2, seq=1300, top_k=5),
+    # one partial query tile over one partial key block
+    "bf16_t50": lambda: small_cfg("p32k", seq=50, top_k=2, n_plants=0),
     "decode_ragged": lambda: small_cfg("d1m", batch=2, seq=5000, top_k=8, n_plants=4),
     "decode_f32": lambda: small_cfg("d1m", batch=3, seq=3001, dtype="f32", top_k=5,
                                     head_dim=64, n_plants=2),
     "decode_short_cache": lambda: small_cfg("d1m", batch=2, seq=200, top_k=64, n_plants=0),
+    "decode_one_key": lambda: small_cfg("d1m", batch=2, seq=1, top_k=4, n_plants=0),
     "decode_g8": lambda: small_cfg("d1m", batch=3, seq=9000, n_heads_q=32, top_k=12,
                                    n_plants=4),
     "decode_g4_k3": lambda: small_cfg("d1m", batch=5, seq=1000, n_heads_q=16, top_k=3,
