@@ -144,6 +144,18 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     s.abort = 0;
     ptx::fence_barrier_init();
+    // the CTA's two Q tiles depend on nothing else: their copy starts before the
+    // selection is read (test hook: no copies at all)
+    if (p.inject != 1) {
+      ptx::tma_prefetch_desc(&tm_q);
+      ptx::mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
+      for (int i = 0; i < 2; ++i) {
+        const int t0 = m * kQt + (part * 2 + i) * tok_per_tile;
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_4d(s.q[i] + kc * kTileRows * kRowBytes, &tm_q, &s.q_full, kc * 64,
+                           g * G, t0, b);
+      }
+    }
   }
   if (warp == 0) {
     ptx::tmem_alloc(&s.tmem_base, kTmemCols);
@@ -176,16 +188,8 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // test hook: issue nothing, so the consumers' bounded waits run out
     const int n_load = p.inject == 1 ? 0 : n_sel;
     if (lane == 0 && n_load > 0) {
-      ptx::tma_prefetch_desc(&tm_q);
       ptx::tma_prefetch_desc(&tm_k);
       ptx::tma_prefetch_desc(&tm_v);
-      ptx::mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
-      for (int i = 0; i < 2; ++i) {
-        const int t0 = m * kQt + (part * 2 + i) * tok_per_tile;
-        for (int kc = 0; kc < 2; ++kc)
-          ptx::tma_load_4d(s.q[i] + kc * kTileRows * kRowBytes, &tm_q, &s.q_full, kc * 64,
-                           g * G, t0, b);
-      }
     }
     for (int j = 0; j < n_load; ++j) {
       const int blk = s.blocks[j];
@@ -205,8 +209,10 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(s, status, 0x201);
+    // the Q copy was issued before anyone knew whether a block would need it: it lands
+    // before the CTA leaves (at once when the MMA warp has used it)
+    if (lane == 0 && p.inject != 1) ptx::mbar_wait_timed(&s.q_full, 0);
     if (*abort && lane == 0 && n_load > 0) {
-      ptx::mbar_wait_timed(&s.q_full, 0);
       for (int j = k_issued > kKStages ? k_issued - kKStages : 0; j < k_issued; ++j)
         ptx::mbar_wait_timed(&s.k_full[j % kKStages], (j / kKStages) & 1);
       for (int j = v_issued > kVStages ? v_issued - kVStages : 0; j < v_issued; ++j)
