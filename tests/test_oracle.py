@@ -6,6 +6,27 @@ import oracle
 from tests.oracle_pins import ALL_PINS
 
 
+
+@pytest.fixture(autouse=True)
+def _one_thread_per_library():
+    """The pins' problems are tiny: BLAS and torch run them on one thread, so their float64
+    results do not depend on how a library splits a product across threads."""
+    import torch
+    n = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    try:
+        if threadpool_limits is None:
+            yield
+        else:
+            with threadpool_limits(limits=1, user_api="blas"):
+                yield
+    finally:
+        torch.set_num_threads(n)
+
 @pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
 def test_oracle_pin(pin):
     pin(oracle.msa_oracle)

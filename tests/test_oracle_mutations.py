@@ -13,6 +13,26 @@ ORACLE_SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file
                           "oracle", "msa_oracle.py")
 
 
+@pytest.fixture(autouse=True)
+def _one_thread_per_library():
+    """The pins' problems are tiny: BLAS and torch run them on one thread, so their float64
+    results do not depend on how a library splits a product across threads."""
+    import torch
+    n = torch.get_num_threads()
+    torch.set_num_threads(1)
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    try:
+        if threadpool_limits is None:
+            yield
+        else:
+            with threadpool_limits(limits=1, user_api="blas"):
+                yield
+    finally:
+        torch.set_num_threads(n)
+
 def _fresh_oracle():
     spec = importlib.util.spec_from_file_location("msa_oracle_mutant", ORACLE_SRC)
     mod = importlib.util.module_from_spec(spec)
