@@ -98,6 +98,117 @@ def pin_decode_scores_bruteforce(o):
     assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
+def _pooled_matmul(q, k, scale, bs, qt, q_pos):
+    """Block scores from one dense numpy product: s = scale * q k^T for every (query, key),
+    -inf where key > query position, padded with -inf to whole tiles and blocks, then the
+    max over each (tile, block) rectangle.  q [B, n, NI, dI] at positions q_pos[n]; k
+    [B, L, dI].  Returns [B, NI, ceil(n/qt), ceil(L/bs)]."""
+    B, n, NI, _ = q.shape
+    L = k.shape[1]
+    s = scale * np.einsum("bngc,bjc->bgnj", q, k)
+    s = np.where(np.arange(L)[None, None, None, :] <= np.asarray(q_pos)[None, None, :, None],
+                 s, -np.inf)
+    nT, nB = -(-n // qt), -(-L // bs)
+    full = np.full((B, NI, nT * qt, nB * bs), -np.inf)
+    full[:, :, :n, :L] = s
+    return full.reshape(B, NI, nT, qt, nB, bs).max(axis=(3, 5))
+
+
+def _check_scores_equal(got, ref):
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    assert np.allclose(got[fin], ref[fin], rtol=1e-12, atol=1e-12)
+
+
+def pin_scores_many_blocks(o):
+    """The oracle scores long key ranges a chunk of whole blocks at a time.  Prefill and
+    decode with more blocks than one chunk holds (several hundred), ragged last tile and
+    block, equal one dense masked product pooled by reshaping; so do small cases with the
+    chunk forced to 1 and 3 blocks, where every chunk boundary cuts a tile's key range."""
+    r = _rng(51)
+    q, k = r.standard_normal((1, 601, 2, 3)), r.standard_normal((1, 601, 3))
+    _check_scores_equal(o.index_block_scores_prefill(q, k, 2, 2, 0.3),
+                        _pooled_matmul(q, k, 0.3, 2, 2, np.arange(601)))
+    qd, kd = r.standard_normal((2, 1, 2, 3)), r.standard_normal((2, 701, 3))
+    _check_scores_equal(o.index_block_scores_decode(qd, kd, 2, 0.3)[:, :, 0],
+                        _pooled_matmul(qd, kd, 0.3, 2, 1, [700])[:, :, 0])
+    saved = o._BLOCKS_PER_CHUNK
+    try:
+        for chunk in (1, 3):
+            o._BLOCKS_PER_CHUNK = chunk
+            q, k = r.standard_normal((2, 37, 3, 4)), r.standard_normal((2, 37, 4))
+            _check_scores_equal(o.index_block_scores_prefill(q, k, 4, 2, 0.7),
+                                _pooled_matmul(q, k, 0.7, 4, 2, np.arange(37)))
+            qd, kd = r.standard_normal((1, 1, 3, 4)), r.standard_normal((1, 23, 4))
+            _check_scores_equal(o.index_block_scores_decode(qd, kd, 4, 0.7)[:, :, 0],
+                                _pooled_matmul(qd, kd, 0.7, 4, 1, [22])[:, :, 0])
+    finally:
+        o._BLOCKS_PER_CHUNK = saved
+
+
+def pin_sampled_forward_equals_full(o):
+    """The oracle's sampled evaluation (a list of query tiles) of the scores, the selection,
+    the attention and the whole prefill returns exactly the full evaluation's values on
+    those tiles, whatever order the tiles are listed in."""
+    r = _rng(52)
+    B, T, Hq, Hkv, d, dI, bs, qt, kk = 2, 45, 4, 2, 3, 5, 8, 4, 3
+    q, k, v = (r.standard_normal((B, T, Hq, d)), r.standard_normal((B, Hkv, T, d)),
+               r.standard_normal((B, Hkv, T, d)))
+    iq, ik = r.standard_normal((B, T, Hkv, dI)), r.standard_normal((B, T, dI))
+    tiles = [9, 0, 4, 11]
+    rows = np.concatenate([np.arange(m * qt, min(T, (m + 1) * qt)) for m in tiles])
+    sc_f, sel_f, out_f, lse_f = o.msa_prefill(q, k, v, iq, ik, bs, qt, kk)
+    sc_s, sel_s, out_s, lse_s = o.msa_prefill(q, k, v, iq, ik, bs, qt, kk, tiles=tiles)
+    assert np.array_equal(sc_s, sc_f[:, :, tiles])
+    assert np.array_equal(sel_s, sel_f[:, :, tiles])
+    assert np.array_equal(out_s, out_f[:, rows]) and np.array_equal(lse_s, lse_f[:, :, rows])
+    assert np.array_equal(o.index_block_scores_prefill(iq, ik, bs, qt, None, tiles),
+                          sc_f[:, :, tiles])
+    assert np.array_equal(o.block_topk_prefill(sc_f[:, :, tiles], T, qt, bs, kk, tiles),
+                          sel_f[:, :, tiles])
+    out_a, lse_a = o.sparse_attention(q, k, v, sel_f, bs, qt, None, 0, tiles)
+    assert np.array_equal(out_a, out_f[:, rows]) and np.array_equal(lse_a, lse_f[:, :, rows])
+
+
+def pin_shared_selection_f32_sum(o):
+    """The aggregated selection of the ablation: per (sequence, row), the KV heads' scores
+    summed in float32 in head order, then the usual rule.  Checked against a loop that adds
+    numpy float32 scalars and ranks with Python's sorted(); one row is built so that the
+    float32 sum and the exact sum rank two blocks the other way round, and one so that a
+    max over the heads would choose differently from their sum."""
+    r = _rng(53)
+    B, NI, T, qt, bs, kk = 2, 4, 40, 4, 4, 2
+    nT, nB = T // qt, T // bs
+    sc = r.integers(-4, 5, size=(B, NI, nT, nB)).astype(np.float64)
+    # row (0, 9): cur = 9; block 2 sums to 1e8 in float32 (1e8 + 6 exactly), block 5 to
+    # 1e8 + 8 in float32 (1e8 + 5 exactly); the others are far lower; one block besides
+    # the current one is kept
+    sc[0, :, 9, :] = -50.0
+    sc[0, :, 9, 2] = [1e8, 3.0, 3.0, 0.0]
+    sc[0, :, 9, 5] = [1e8, 5.0, 0.0, 0.0]
+    # row (1, 7): cur = 7; block 1 has the larger maximum, block 3 the larger sum
+    sc[1, :, 7, :] = -50.0
+    sc[1, :, 7, 1] = [9.0, 0.0, 0.0, 0.0]
+    sc[1, :, 7, 3] = [3.0, 3.0, 3.0, 3.0]
+    got = o.block_topk_shared_prefill(sc, T, qt, bs, kk)
+    for b in range(B):
+        for m in range(nT):
+            agg = []
+            for blk in range(nB):
+                acc = np.float32(sc[b, 0, m, blk])
+                for g in range(1, NI):
+                    acc = np.float32(acc + np.float32(sc[b, g, m, blk]))
+                agg.append(float(acc))
+            cur = (m * qt + qt - 1) // bs
+            best = [blk for _, blk in sorted((-agg[blk], blk) for blk in range(cur))][:kk - 1]
+            want = sorted(best + [cur])
+            want += [-1] * (kk - len(want))
+            for g in range(NI):
+                assert list(got[b, g, m]) == want, (b, g, m, got[b, g, m], want)
+    assert list(got[0, 0, 9]) == [5, 9] and list(got[1, 0, 7]) == [3, 7]
+
+
 # ----------------------------------------------------------------------- top-k
 
 def _dominates(scores, chosen, cur):
@@ -544,6 +655,7 @@ def pin_index_kl_group_mean(o):
 
 ALL_PINS = [
     pin_scores_block1_tile1, pin_scores_bruteforce, pin_decode_scores_bruteforce,
+    pin_scores_many_blocks, pin_sampled_forward_equals_full, pin_shared_selection_f32_sum,
     pin_topk_bruteforce, pin_topk_layout, pin_full_k_bruteforce, pin_full_k_sdpa,
     pin_sparse_bruteforce, pin_rows_sum_to_one, pin_unselected_invariance,
     pin_decode_equals_prefill_row, pin_planted_selected, pin_head_diversity,

@@ -171,10 +171,54 @@ def _mut_kl_first_head_target(o):
     o.index_kl_loss = index_kl_loss
 
 
+def _mut_chunk_keys_from_zero(o):
+    # every chunk of index keys masked as if it started at key 0 (causality broken for
+    # every chunk after the first)
+    base = o.index_logits
+    o.index_logits = lambda qr, kk, sc, pos, key_pos0=0: base(qr, kk, sc, pos, 0)
+
+
+def _mut_shared_max(o):
+    # the shared selection ranks by the heads' maximum instead of their sum
+    base = o.block_topk_shared_prefill
+
+    def block_topk_shared_prefill(scores, seq_len, q_tile, block_size, top_k):
+        sc = np.asarray(scores, dtype=np.float64)
+        mx = np.repeat(sc.max(axis=1, keepdims=True), sc.shape[1], axis=1)
+        return base(mx / sc.shape[1], seq_len, q_tile, block_size, top_k)
+    o.block_topk_shared_prefill = block_topk_shared_prefill
+
+
+def _mut_shared_exact_sum(o):
+    # the shared selection ranks by the exact (float64) sum, not the float32 one
+    def block_topk_shared_prefill(scores, seq_len, q_tile, block_size, top_k):
+        sc = np.asarray(scores, dtype=np.float64)
+        one = o.block_topk_prefill(sc.sum(axis=1, keepdims=True), seq_len, q_tile,
+                                   block_size, top_k)
+        return np.repeat(one, sc.shape[1], axis=1)
+    o.block_topk_shared_prefill = block_topk_shared_prefill
+
+
+def _mut_sampled_tile_position(o):
+    # a sampled evaluation reads the selection row of the tile's place in the list
+    # instead of the tile's own row
+    base = o.sparse_attention
+
+    def sparse_attention(q, k, v, sel, block_size, q_tile, sm_scale=None, q_offset=0,
+                         tiles=None):
+        if tiles is not None:
+            sel = np.array(sel)
+            rows = [int(m) for m in tiles]
+            sel[:, :, rows] = np.array(sel)[:, :, list(range(len(rows)))]
+        return base(q, k, v, sel, block_size, q_tile, sm_scale, q_offset, tiles)
+    o.sparse_attention = sparse_attention
+
+
 MUTATIONS = [_mut_strict_mask, _mut_no_index_scale, _mut_mean_pool, _mut_ties_high,
              _mut_no_forced_current, _mut_unsorted_output, _mut_current_block_first_query,
              _mut_block_keys_short, _mut_strided_groups, _mut_transposed_index,
-             _mut_backward_no_D, _mut_kl_first_head_target]
+             _mut_backward_no_D, _mut_kl_first_head_target, _mut_chunk_keys_from_zero,
+             _mut_shared_max, _mut_shared_exact_sum, _mut_sampled_tile_position]
 
 
 @pytest.mark.parametrize("mutate", MUTATIONS, ids=[m.__name__[5:] for m in MUTATIONS])
