@@ -122,9 +122,10 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
   for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
+  int issued = 0;                                          // producer: copies issued
   if (warp == kComputeWarps) {
     // ------------------------------------------------------------- TMA producer
-    int j = 0;
+    int& j = issued;
     bool ok = true;
     for (int i = i0; i < i1; ++i) {
       const int blk = block_at(i);
@@ -149,9 +150,6 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
       s.abort = 1;
       if (status) atomicExch(status, 0x401);
     }
-    if (*abort && lane == 0)
-      for (int x = j > kStages ? j - kStages : 0; x < j; ++x)
-        ptx::mbar_wait_timed(&s.full[x % kStages], (x / kStages) & 1);
   } else {
     // ------------------------------------------------------------ compute warps
     const int gr = lane >> 2, c = lane & 3;                  // fragment row / column pair
@@ -255,7 +253,14 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
       if (status) atomicExch(status, 0x402);
     }
   }
-  // every copy into the ring has landed (the producer drained any in flight on abort)
+  // Every warp has left its loop, so the abort flag is final.  Without an abort the compute
+  // warps consumed every copy; after one (set by the producer or by a compute warp that gave
+  // up), the producer waits for its last copies, which may still be in flight, before the
+  // ring's memory is reused for the merge.
+  __syncthreads();
+  if (warp == kComputeWarps && lane == 0 && *abort)
+    for (int x = issued > kStages ? issued - kStages : 0; x < issued; ++x)
+      ptx::mbar_wait_timed(&s.full[x % kStages], (x / kStages) & 1);
   __syncthreads();
   if (warp < kComputeWarps) {
     const int gr = lane >> 2, c = lane & 3;

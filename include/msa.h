@@ -48,6 +48,10 @@
  *     msa_get_device_status() reports as MSA_ERR_TIMEOUT.
  *   - Inputs must be finite; NaN scores give an unspecified (but in-range) selection.
  *   - Calls on distinct streams may run concurrently; the device status word is shared.
+ *   - The library looks up the device addresses of its own device variables (the status
+ *     word, the static decode scratch) once per device and caches them.  cudaDeviceReset
+ *     (or any other teardown of the primary context) leaves those addresses stale: using
+ *     the library in the same process after a device reset is not supported.
  */
 #ifndef MSA_H_
 #define MSA_H_

@@ -9,8 +9,9 @@ Tolerances (written here once, used by every parity test):
 * gradients (dq, dk, dv of the sparse attention): rel-L2 <= 1e-4 for fp32 inputs; for bf16
   rel-L2 <= 1e-2, because the backward uses the forward output rounded to bf16 in
   D = dout . out (relative 2^-9 per element), and max-abs <= 5e-2 of the largest |ref|;
-* selections: bit-exact where both sides rank the same fp32 scores; where the oracle
-  ranks its own fp64 scores, a differing choice must be one a score tolerance allows.
+* selections: bit-exact against the oracle's top-k run on the GPU's own fp32 block scores;
+  against the oracle's selection from its own fp64 scores, a differing choice must be one
+  the score tolerance allows (the agreement rate is reported).
 """
 from __future__ import annotations
 
@@ -92,6 +93,15 @@ def check_grad(gpu, ref, dtype, what="grad"):
     assert rel <= rtol and mx <= atol, f"{what}: rel-L2 {rel:.3g} (<= {rtol}), " \
         f"max-abs / max|ref| {mx:.3g} (<= {atol})"
     return rel, mx
+
+
+def check_selection_exact(gpu_sel, ref_sel, what="sel"):
+    """Bit-exact selection: both sides ranked the same fp32 scores."""
+    gpu_sel, ref_sel = to_np(gpu_sel), np.asarray(ref_sel)
+    assert gpu_sel.shape == ref_sel.shape, (gpu_sel.shape, ref_sel.shape)
+    bad = np.argwhere(np.any(gpu_sel != ref_sel, axis=-1))
+    assert bad.size == 0, f"{what}: {len(bad)} selection rows differ, e.g. " \
+        f"{bad[:2].tolist()}: {gpu_sel[tuple(bad[0])]} vs {ref_sel[tuple(bad[0])]}"
 
 
 def check_selection_valid(gpu_sel, ref_sel, ref_scores, cur_blocks, what="sel"):

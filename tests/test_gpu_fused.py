@@ -7,7 +7,8 @@ import oracle
 from block_sparse_gqa_02_gb300 import _lib
 from block_sparse_gqa_02_gb300.configs import CONFIGS
 from block_sparse_gqa_02_gb300.inputs import make_inputs
-from tests.parity import check_scores, check_selection_valid, sample_tiles, to_np
+from tests.parity import (check_scores, check_selection_exact, check_selection_valid,
+                          sample_tiles, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -44,8 +45,12 @@ def test_fused_matches_two_calls_and_oracle(name):
     ref_sc = oracle.index_block_scores_prefill(x["idx_q"], x["idx_k"], 128, 64, tiles=tiles)
     ref_sel = oracle.block_topk_prefill(ref_sc, cfg.seq, 64, 128, cfg.top_k, tiles=tiles)
     r_idx = torch.tensor(tiles, device="cuda")
-    check_scores(to_np(sc1.index_select(2, r_idx)), ref_sc, name)
+    g_sc = to_np(sc1.index_select(2, r_idx))
+    check_scores(g_sc, ref_sc, name)
     cb = np.array([(min(cfg.seq - 1, m * 64 + 63)) // 128 for m in tiles])
     g_sel = to_np(sel0.index_select(2, r_idx))
+    # bit-exact against the oracle's top-k on the GPU's own fp32 scores
+    check_selection_exact(g_sel, oracle.block_topk_prefill(g_sc, cfg.seq, 64, 128, cfg.top_k,
+                                                           tiles=tiles), name)
     assert check_selection_valid(g_sel, ref_sel, ref_sc,
                                  np.broadcast_to(cb, g_sel.shape[:-1]), name) >= 0.9

@@ -8,7 +8,8 @@ import oracle
 from block_sparse_gqa_02_gb300 import _lib
 from block_sparse_gqa_02_gb300.configs import CONFIGS
 from block_sparse_gqa_02_gb300.inputs import make_paged_decode_inputs
-from tests.parity import check_lse, check_out, check_scores, check_selection_valid, to_np
+from tests.parity import (check_lse, check_out, check_scores, check_selection_exact,
+                          check_selection_valid, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,12 +57,23 @@ def test_paged_ragged_decode(name):
     agree = check_selection_valid(g_sel, sel, sc, np.broadcast_to(cb, g_sel.shape[:-1]), name)
     assert agree >= 0.9
     for b, L in enumerate(lens):
-        for g in range(4):
-            if not np.array_equal(g_sel[b, g, 0], sel[b, g, 0]):
-                continue
-            hs = np.arange(g * 16, (g + 1) * 16)
-            check_out(g_o[b, 0, hs], o[b, 0, hs], "bf16", f"{name} seq {b}")
-            check_lse(g_l[b, hs], l[b, hs], "bf16", f"{name} seq {b}")
+        if L == 0:
+            continue
+        # the selection bit-exactly against the oracle's top-k on the GPU's own fp32 scores
+        # of this sequence's blocks; then the attention over the GPU's selection, on the
+        # sequence's logical cache (the input pools' blocks in block-table order; the oracle
+        # reads only the selected keys)
+        nb = -(-L // 128)
+        check_selection_exact(g_sel[b:b + 1],
+                              oracle.block_topk_decode(g_sc[b:b + 1, :, :, :nb], L, 128,
+                                                       cfg.top_k), f"{name} seq {b}")
+        phys = x["block_table"][b, :nb].long()
+        kc, vc = (x[n][phys].transpose(0, 1).reshape(4, nb * 128, -1)[:, :L]
+                  for n in ("k_pool", "v_pool"))        # [Hkv, L, d], inputs rearranged
+        ref_o, ref_l = oracle.sparse_attention(x["q"][b:b + 1], kc[None], vc[None],
+                                               g_sel[b:b + 1], 128, 1, None, L - 1)
+        check_out(g_o[b:b + 1], ref_o, "bf16", f"{name} seq {b}")
+        check_lse(g_l[b:b + 1], ref_l, "bf16", f"{name} seq {b}")
     # an empty sequence selects nothing and attends to nothing
     for b, L in enumerate(lens):
         if L == 0:

@@ -6,8 +6,10 @@ allocate after start-up.  msa_sparse_decode_static serves them: it takes no work
 keeps the split-KV partial results in a scratch array the library holds on the device.
 These tests call it through the C ABI twice in a row (the second call on a different
 shape, so it runs over the first call's leftovers) and compare each result with the
-regular msa_sparse_decode on the same inputs, within the bf16 output tolerance the parity
-tests use.  The file is named so pytest collects it last.
+regular msa_sparse_decode on the same inputs.  Both entry points run the same kernels in
+the same order on the same inputs, so their outputs must be bit-identical (which also puts
+them within the bf16 output tolerance the parity tests use).  The file is named so pytest
+collects it last.
 """
 import ctypes
 
@@ -49,6 +51,8 @@ def test_static_scratch_decode_matches_regular_twice():
     second = CONFIGS["d1m"].with_(batch=3, seq=70_001, top_k=24, n_plants=5, seed=11)
     for cfg, seed in ((first, 1), (second, 2)):
         out, lse, out_ref, lse_ref = _decode_both(cfg, seed)
+        assert np.array_equal(out, out_ref), f"static decode {cfg.batch}x{cfg.seq}: out differs"
+        assert np.array_equal(lse, lse_ref), f"static decode {cfg.batch}x{cfg.seq}: lse differs"
         check_out(out, out_ref, "bf16", f"static decode {cfg.batch}x{cfg.seq}")
         check_lse(lse, lse_ref, "bf16", f"static decode {cfg.batch}x{cfg.seq}")
 
