@@ -68,11 +68,12 @@ def decode_bytes(cfg):
 # that was profiled: a changed kernel reports null until it is captured again.
 MEASURED_TRAFFIC = {
     "sparse_prefill_tc.cu": {
-        "sha256_16": "6a57956284ac2fb8",
+        "sha256_16": "8a014b486aafd2d6",
         "workload": "p128k",
         "bytes_per_launch": 4.53e9,
-        "how": "dram__bytes_read.sum + dram__bytes_write.sum of one p32k launch "
-               "(336.1 + 229.8 MB), scaled by the (token, query head) rows to 128K (x8)",
+        "how": "dram__bytes_read.sum + dram__bytes_write.sum of one launch at 65536 tokens "
+               "with the 128K config's heads (1220.3 + 1044.8 MB), scaled by the (token, query "
+               "head) rows to 128K (x2)",
     },
     "index_scan_tc.cu": {
         "sha256_16": "86e08ca0ed2ffa41",
@@ -536,6 +537,11 @@ def run_ours(args, rank, world, device):
     torch.cuda.set_device(device)
     _lib.load()
     pcfg = CONFIGS[args.prefill]
+    if args.prefill_seq or args.prefill_heads:
+        seq = args.prefill_seq or pcfg.seq
+        hq = args.prefill_heads or pcfg.n_heads_q
+        pcfg = pcfg.with_(seq=seq, n_heads_q=hq, name=f"{pcfg.name}-T{seq}-H{hq}",
+                          description=f"{pcfg.description} (T={seq}, {hq} query heads)")
     dcfg = CONFIGS[args.decode]
     if args.decode_len:
         dcfg = dcfg.with_(seq=args.decode_len, name=f"{dcfg.name}-L{args.decode_len}",
@@ -775,6 +781,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["msa", "reference"], default="msa")
     ap.add_argument("--prefill", default="p128k", choices=["p32k", "p128k", "p1m"])
+    ap.add_argument("--prefill-seq", type=int, default=0,
+                    help="override the prefill sequence length (smaller cases for profiling)")
+    ap.add_argument("--prefill-heads", type=int, default=0,
+                    help="override the prefill query-head count (smaller cases for profiling)")
     ap.add_argument("--decode", default="d1m", choices=["d1m"])
     ap.add_argument("--decode-len", type=int, default=0,
                     help="override the decode cache length (smaller cases for profiling)")

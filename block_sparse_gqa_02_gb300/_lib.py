@@ -10,7 +10,8 @@ import ctypes
 import os
 import threading
 
-MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_CUDA, MSA_ERR_TIMEOUT = range(5)
+(MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_CUDA, MSA_ERR_TIMEOUT,
+ MSA_ERR_BOUNDS) = range(6)
 MSA_F32, MSA_BF16 = 0, 1
 _DTYPE_CODES = {"f32": MSA_F32, "bf16": MSA_BF16}
 
@@ -59,11 +60,17 @@ SIGNATURES = {
     "msa_status_string": (ctypes.c_char_p, [_i32]),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_abi_version": (_i32, []),
+    "msa_debug_build": (_i32, []),
     "msa_debug_set_fault": (_i32, [_i32]),
 }
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}                 # variant -> loaded library
+# The variant the calls below go through: "release" (libmsa.so), or "debug"
+# (libmsa_debug.so, built with the device-side index checks) when the environment sets
+# MSA_LIBRARY_VARIANT=debug.  A process loads one variant: the two libraries export the same
+# symbols and device variables.
+_active = os.environ.get("MSA_LIBRARY_VARIANT", "release")
 
 
 class MsaError(RuntimeError):
@@ -72,19 +79,26 @@ class MsaError(RuntimeError):
         super().__init__(f"{where}: status {status} ({detail})")
 
 
-def library_path() -> str:
-    return os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmsa.so")
+def library_path(variant: str = "release") -> str:
+    name = "libmsa.so" if variant == "release" else f"libmsa_{variant}.so"
+    return os.path.join(os.path.dirname(os.path.abspath(__file__)), name)
 
 
-def load(build_if_missing: bool = True):
-    """The loaded library (built in-tree with nvcc on first use if needed)."""
-    global _lib
+def load(build_if_missing: bool = True, variant: str | None = None):
+    """The loaded library of `variant` (default: the process's variant, see
+    MSA_LIBRARY_VARIANT), built in-tree with nvcc on first use if needed."""
+    variant = _active if variant is None else variant
+    if variant not in ("release", "debug"):
+        raise ValueError(f"unknown MSA library variant {variant!r}")
     with _lock:
-        if _lib is None:
-            path = library_path()
+        if _libs and variant not in _libs:
+            raise RuntimeError(f"the {next(iter(_libs))} MSA library is already loaded in this "
+                               f"process; run the {variant} variant in a process of its own")
+        if variant not in _libs:
+            path = library_path(variant)
             if build_if_missing:
                 from . import build as _build
-                path = _build.build()
+                path = _build.build(variant=variant)
             if not os.path.exists(path):
                 raise RuntimeError(f"MSA CUDA library missing at {path}; run the build first")
             lib = ctypes.CDLL(path)
@@ -92,8 +106,8 @@ def load(build_if_missing: bool = True):
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
-            _lib = lib
-        return _lib
+            _libs[variant] = lib
+        return _libs[variant]
 
 
 def _ptr(x):

@@ -2,7 +2,9 @@
 
 Every translation unit under csrc/ is compiled in parallel (one -gencode, no cmake) and
 linked into block_sparse_gqa_02_gb300/libmsa.so.  A stamp of the sources, headers and
-flags skips the build when nothing changed.
+flags skips the build when nothing changed.  The debug variant (-DMSA_DEBUG: device-side
+index checks, see msa_debug_build in include/msa.h) builds the same sources into
+libmsa_debug.so, in a build folder of its own.
 """
 from __future__ import annotations
 
@@ -19,6 +21,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmsa.so")
+VARIANTS = {
+    "release": (BUILD, LIB, []),
+    "debug": (os.path.join(PKG, "_build_debug"), os.path.join(PKG, "libmsa_debug.so"),
+              ["-DMSA_DEBUG"]),
+}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -48,20 +55,24 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, extra_flags=(), force: bool = False) -> str:
-    """Compile csrc/*.cu and link libmsa.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
-    stamp_path = os.path.join(BUILD, "stamp")
+def build(verbose: bool = False, extra_flags=(), force: bool = False,
+          variant: str = "release") -> str:
+    """Compile csrc/*.cu and link the library of `variant` ("release": libmsa.so, "debug":
+    libmsa_debug.so); returns the library path."""
+    build_dir, lib_path, variant_flags = VARIANTS[variant]
+    extra_flags = list(variant_flags) + list(extra_flags)
+    os.makedirs(build_dir, exist_ok=True)
+    stamp_path = os.path.join(build_dir, "stamp")
     stamp = _stamp(extra_flags)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp_path):
+    if not force and os.path.exists(lib_path) and os.path.exists(stamp_path):
         with open(stamp_path) as f:
             if f.read() == stamp:
-                return LIB
+                return lib_path
     nvcc = _nvcc()
     flags = NVCC_FLAGS + list(extra_flags)
 
     def compile_one(src):
-        obj = os.path.join(BUILD, src[:-3] + ".o")
+        obj = os.path.join(build_dir, src[:-3] + ".o")
         cmd = [nvcc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -72,17 +83,19 @@ def build(verbose: bool = False, extra_flags=(), force: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":
-    extra = sys.argv[1:]
-    print(build(verbose=True, extra_flags=extra, force=True))
+    args = sys.argv[1:]
+    variant = "debug" if "--debug" in args else "release"
+    extra = [a for a in args if a != "--debug"]
+    print(build(verbose=True, extra_flags=extra, force=True, variant=variant))

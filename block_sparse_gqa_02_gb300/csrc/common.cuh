@@ -25,6 +25,37 @@ struct Dims {
   int n_phys;
 };
 
+// ------------------------------------------------------------ debug checks
+// A build with -DMSA_DEBUG checks indices on the device: every selection entry, block-table
+// entry and cache length a call receives (launch_debug_validate), and the coordinates the
+// tensor-core kernels give their tensor copies.  A failed check records a code 0xBxx in the
+// device status word (reported as MSA_ERR_BOUNDS; the kernels' timeout codes use other
+// ranges) and never traps; release builds compile the checks away.
+#ifdef MSA_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+constexpr int kDebugCodeBase = 0xB00;
+enum DebugCode : int {
+  kDbgSelRange = 0xB01,       // a selection entry outside [-1, blocks of the sequence)
+  kDbgSelDuplicate = 0xB02,   // a block listed twice in one selection row
+  kDbgTableRange = 0xB03,     // a block-table entry outside [0, n_phys)
+  kDbgSeqLen = 0xB04,         // a cache length outside [0, seq_k]
+  kDbgCoord = 0xB05,          // a tensor-copy coordinate outside its tensor
+  kDbgStore = 0xB06,          // an output index outside its tensor
+};
+
+__device__ __forceinline__ void debug_check(bool ok, int* status, int code) {
+  if (kDebugChecks && !ok && status) atomicCAS(status, 0, code);
+}
+
+// Debug builds: validates the selection rows (sel may be null), block table and cache
+// lengths of a call on the device before its kernels run.  Release builds: does nothing.
+cudaError_t launch_debug_validate(const Dims& p, const int32_t* sel, cudaStream_t st,
+                                  int* status);
+
 // Cache length of sequence b (the decode query sits at position len - 1).
 __device__ __forceinline__ int seq_len_of(const Dims& p, int b) {
   if (!p.seq_lens) return p.Sk;

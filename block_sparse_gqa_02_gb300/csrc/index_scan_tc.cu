@@ -157,6 +157,9 @@ index_scan_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __nv_bfloat
         const int blk = blk0 + i;
         const int y = p.block_table ? 0 : blk * kBk;
         const int z = p.block_table ? p.block_table[(size_t)b * p.nB + blk] : b;
+        debug_check(blk >= 0 && blk < p.nB && y >= 0 && y < p.Sk && z >= 0 &&
+                        z < (p.block_table ? p.n_phys : p.B),
+                    status, kDbgCoord);
         for (int kc = 0; kc < 2; ++kc)
           ptx::tma_load_3d(s.a[st] + kc * kBk * kRowBytes, &tm_k, &s.full[st], kc * 64, y, z);
       }

@@ -210,6 +210,10 @@ msa_status msa_sparse_prefill(const msa_shape* shape, const void* q, const void*
   MSA_TRY(check_ptr(sel, "sel"));
   MSA_TRY(check_ptr(out, "out"));
   MSA_TRY(check_ptr(lse, "lse", true));
+  {
+    const cudaError_t ve = launch_debug_validate(d, sel, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_sparse_prefill debug validation");
+  }
   cudaError_t e = launch_sparse_prefill(d, q, k, v, sel, out, lse, (cudaStream_t)stream,
                                         status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_prefill launch");
@@ -241,6 +245,10 @@ msa_status msa_sparse_prefill_backward(const msa_shape* shape, const void* q, co
     if (ws_bytes < need)
       return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, need);
   }
+  {
+    const cudaError_t ve = launch_debug_validate(d, sel, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_sparse_prefill_backward debug validation");
+  }
   cudaError_t e = launch_sparse_prefill_backward(d, q, k, v, sel, out, lse, dout, dq, dk, dv,
                                                  workspace, (cudaStream_t)stream, status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_prefill_backward launch");
@@ -271,6 +279,10 @@ msa_status msa_index_kl_loss(const msa_shape* shape, const void* q, const void* 
     if (ws_bytes < need)
       return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes, need %zu", ws_bytes, need);
   }
+  {
+    const cudaError_t ve = launch_debug_validate(d, sel, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_index_kl_loss debug validation");
+  }
   cudaError_t e = launch_index_kl(d, q, k, lse, idx_q, idx_k, sel, loss, d_idx_q, d_idx_k,
                                   workspace, (cudaStream_t)stream, status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_kl_loss launch");
@@ -295,6 +307,10 @@ msa_status msa_sparse_decode(const msa_shape* shape, const void* q, const void* 
   if (ws_bytes < need)
     return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes is too small: need %zu", ws_bytes,
                 need);
+  {
+    const cudaError_t ve = launch_debug_validate(d, sel, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_sparse_decode debug validation");
+  }
   cudaError_t e = launch_sparse_decode(d, q, k_cache, v_cache, sel, out, lse,
                                        static_cast<float*>(workspace), (cudaStream_t)stream,
                                        status_ptr());
@@ -335,6 +351,10 @@ msa_status msa_index_scores_paged(const msa_shape* shape, const int32_t* seq_len
   MSA_TRY(check_ptr(idx_q, "idx_q"));
   MSA_TRY(check_ptr(idx_k_pool, "idx_k_pool"));
   MSA_TRY(check_ptr(block_scores, "block_scores"));
+  {
+    const cudaError_t ve = launch_debug_validate(d, nullptr, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_index_scores_paged debug validation");
+  }
   cudaError_t e = launch_index_scores(d, idx_q, idx_k_pool, block_scores, (cudaStream_t)stream,
                                       status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_index_scores_paged launch");
@@ -350,6 +370,10 @@ msa_status msa_block_topk_ragged(const msa_shape* shape, const int32_t* seq_lens
   MSA_TRY(check_ptr(block_scores, "block_scores"));
   MSA_TRY(check_ptr(sel, "sel"));
   d.seq_lens = seq_lens;
+  {
+    const cudaError_t ve = launch_debug_validate(d, nullptr, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_block_topk_ragged debug validation");
+  }
   cudaError_t e = launch_block_topk(d, block_scores, sel, (cudaStream_t)stream);
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_block_topk_ragged launch");
 }
@@ -373,6 +397,10 @@ msa_status msa_sparse_decode_paged(const msa_shape* shape, const int32_t* seq_le
   if (ws_bytes < need)
     return fail(MSA_ERR_INVALID_ARG, "workspace of %zu bytes is too small: need %zu", ws_bytes,
                 need);
+  {
+    const cudaError_t ve = launch_debug_validate(d, sel, (cudaStream_t)stream, status_ptr());
+    if (ve != cudaSuccess) return cuda_fail(ve, "msa_sparse_decode_paged debug validation");
+  }
   cudaError_t e = launch_sparse_decode(d, q, k_pool, v_pool, sel, out, lse,
                                        static_cast<float*>(workspace), (cudaStream_t)stream,
                                        status_ptr());
@@ -400,6 +428,9 @@ msa_status msa_get_device_status(void* stream) {
   if (code != 0) {
     const int zero = 0;
     cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    if ((code & ~0xff) == kDebugCodeBase)
+      return fail(MSA_ERR_BOUNDS, "a debug-build check found an index out of range (code %#x)",
+                  code);
     return fail(MSA_ERR_TIMEOUT, "a kernel gave up a bounded wait (code %d)", code);
   }
   return MSA_OK;
@@ -412,6 +443,7 @@ const char* msa_status_string(msa_status status) {
     case MSA_ERR_UNSUPPORTED: return "MSA_ERR_UNSUPPORTED: shape not supported";
     case MSA_ERR_CUDA: return "MSA_ERR_CUDA: CUDA error";
     case MSA_ERR_TIMEOUT: return "MSA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+    case MSA_ERR_BOUNDS: return "MSA_ERR_BOUNDS: a debug-build index check failed";
   }
   return "unknown msa_status";
 }
@@ -425,6 +457,8 @@ msa_status msa_debug_set_fault(int32_t mode) {
 }
 
 int32_t msa_abi_version(void) { return MSA_ABI_VERSION; }
+
+int32_t msa_debug_build(void) { return kDebugChecks ? 1 : 0; }
 
 }  // extern "C"
 
@@ -497,6 +531,8 @@ extern "C" msa_status msa_sparse_decode_static(const msa_shape* shape, const voi
   if (e != cudaSuccess) return cuda_fail(e, "msa_sparse_decode_static scratch address");
   // Every partial slot the merge reads is written by this call first, so the array's
   // previous contents never matter and nothing needs clearing.
+  e = launch_debug_validate(d, sel, (cudaStream_t)stream, status_ptr());
+  if (e != cudaSuccess) return cuda_fail(e, "msa_sparse_decode_static debug validation");
   e = launch_sparse_decode(d, q, k_cache, v_cache, sel, out, lse, static_cast<float*>(ws),
                            (cudaStream_t)stream, status_ptr());
   return e == cudaSuccess ? MSA_OK : cuda_fail(e, "msa_sparse_decode_static launch");

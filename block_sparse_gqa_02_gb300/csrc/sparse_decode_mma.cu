@@ -138,6 +138,9 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
         // (dims, key in block, physical block*Hkv + g)
         const int y = p.block_table ? 0 : blk * kBk;
         const int z = p.block_table ? p.block_table[(size_t)b * p.nB + blk] * p.Hkv + g : bg;
+        debug_check(y >= 0 && y < p.Sk && z >= 0 &&
+                        z < (p.block_table ? p.n_phys * p.Hkv : p.B * p.Hkv),
+                    status, kDbgCoord);
         for (int kc = 0; kc < 2; ++kc) {
           ptx::tma_load_3d(s.k[st] + kc * kBk * kRowBytes, &tm_k, &s.full[st], kc * 64, y, z);
           ptx::tma_load_3d(s.v[st] + kc * kBk * kRowBytes, &tm_v, &s.full[st], kc * 64, y, z);
@@ -302,6 +305,7 @@ sparse_decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
     const int h = g * G + r;
     if (r < G) {
       const size_t slot = ((size_t)b * p.Hq + h) * n_split + split;
+      debug_check(h < p.Hq && split < n_split, status, kDbgStore);
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
 #pragma unroll
       for (int dd = 0; dd < 16; ++dd) {

@@ -151,6 +151,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_arrive_expect_tx(&s.q_full, 2 * kTileBytes);
       for (int i = 0; i < 2; ++i) {
         const int t0 = m * kQt + (part * 2 + i) * tok_per_tile;
+        debug_check(t0 >= 0 && t0 < p.nR * kQt && bg < p.B * p.Hkv, status, kDbgCoord);
         for (int kc = 0; kc < 2; ++kc)
           ptx::tma_load_4d(s.q[i] + kc * kTileRows * kRowBytes, &tm_q, &s.q_full, kc * 64,
                            g * G, t0, b);
@@ -196,6 +197,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int ks = j % kKStages, vs = j % kVStages;
       if (!ptx::mbar_wait(&s.k_empty[ks], ((j / kKStages) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
+        debug_check(blk >= 0 && blk < p.nB, status, kDbgCoord);
         ptx::mbar_arrive_expect_tx(&s.k_full[ks], kTileBytes);
         ptx::tma_load_4d(s.k[ks], &tm_k, &s.k_full[ks], 0, blk * kBk, 0, bg);
       }
@@ -489,6 +491,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           dst[w] = make_uint4(pk[4 * w], pk[4 * w + 1], pk[4 * w + 2], pk[4 * w + 3]);
       }
     }
+    debug_check(!valid || h < p.Hq, status, kDbgStore);
     if (valid && lse)
       lse[((size_t)b * p.Hq + h) * p.Sq + t] =
           l > 0.f ? (m_used + __log2f(l)) * kLn2 : -INFINITY;

@@ -63,14 +63,16 @@
 extern "C" {
 #endif
 
-#define MSA_ABI_VERSION 1
+#define MSA_ABI_VERSION 2
 
 typedef enum msa_status {
   MSA_OK = 0,
   MSA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, inconsistent or out-of-range shape */
   MSA_ERR_UNSUPPORTED = 2, /* valid shape that no kernel here handles (e.g. head_dim 96) */
   MSA_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
-  MSA_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (device status word) */
+  MSA_ERR_TIMEOUT = 4,     /* a kernel gave up a bounded wait (device status word) */
+  MSA_ERR_BOUNDS = 5       /* debug builds only: a device-side index check failed (device
+                            * status word; see msa_debug_build) */
 } msa_status;
 
 typedef enum msa_dtype { MSA_F32 = 0, MSA_BF16 = 1 } msa_dtype;
@@ -255,6 +257,18 @@ msa_status msa_debug_set_fault(int32_t mode);
 
 /* MSA_ABI_VERSION of the loaded library. */
 int32_t msa_abi_version(void);
+
+/* 1 when the library was built with -DMSA_DEBUG, else 0.  A debug build checks on the
+ * device, before the kernels of each call run, every selection entry it is given (-1 or a
+ * block of the sequence: below ceil(seq_k / block_size), or below ceil(seq_lens[b] /
+ * block_size) for a paged cache; no block twice in a row), every block-table entry of the
+ * sequence's blocks (within [0, n_phys)) and every cache length (within [0, seq_k]); and,
+ * inside the tensor-core kernels, the coordinates of their tensor copies and the indices of
+ * their output stores.  A failed check records a code in the device status word, which
+ * msa_get_device_status() reports as MSA_ERR_BOUNDS; no check traps, and an out-of-range
+ * store is skipped.  Release builds carry none of these checks (they skip selection entries
+ * outside [0, n_blocks) without reporting them). */
+int32_t msa_debug_build(void);
 
 #ifdef __cplusplus
 }

@@ -34,11 +34,12 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert lib.msa_abi_version() == 1
+    assert lib.msa_abi_version() == 2
+    assert lib.msa_debug_build() == 0          # the release build
 
 
 def test_status_strings(lib):
-    for code in range(5):
+    for code in range(6):
         assert lib.msa_status_string(code).startswith(b"MSA_")
 
 
