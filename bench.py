@@ -68,11 +68,11 @@ def decode_bytes(cfg):
 # that was profiled: a changed kernel reports null until it is captured again.
 MEASURED_TRAFFIC = {
     "sparse_prefill_tc.cu": {
-        "sha256_16": "8a014b486aafd2d6",
+        "sha256_16": "588f5883e19a3dce",
         "workload": "p128k",
         "bytes_per_launch": 4.53e9,
         "how": "dram__bytes_read.sum + dram__bytes_write.sum of one launch at 65536 tokens "
-               "with the 128K config's heads (1220.3 + 1044.8 MB), scaled by the (token, query "
+               "with the 128K config's heads (1218.7 + 1045.3 MB), scaled by the (token, query "
                "head) rows to 128K (x2)",
     },
     "index_scan_tc.cu": {

@@ -11,7 +11,11 @@
 // ping-pong on the tensor core (while one tile's softmax runs, the other tile's MMAs do).
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P (bf16) is
 // written over the first 64 columns of S and read by the P.V MMA straight from TMEM.
-// Warps: 0-3 softmax + epilogue of Q tile 0, 4-7 of Q tile 1, 8 TMA producer, 9 MMA issuer.
+// Warps: 0-3 softmax + epilogue of Q tile 0, 4-7 of Q tile 1, 8 TMA producer, 9 issues every
+// Q.K^T and 10 every P.V.  One thread's stream of N = 128 MMAs with commits in it keeps the
+// tensor core busy only ~60 % of the time; two streams that meet only through the barriers
+// (a tile's Q.K^T after its previous P.V, its P.V after its softmax) fill the gaps, and
+// neither issuer ever waits for its own MMAs.
 // Online softmax in the log2 domain with conditional rescaling: the running max used for
 // the exponent only moves when a block would push the row's P past a bound (its sum past
 // 2^9 in a later block; its maximum past 2^8 in a row's first or diagonal block), so the O
@@ -34,9 +38,9 @@ constexpr int kTileBytes = 2 * kTileRows * kRowBytes;   // [2 chunks][128 rows][
 constexpr int kKStages = 2;
 constexpr int kVStages = 2;
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;      // issues the Q.K^T MMAs; warp 10 issues the P.V MMAs
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, kBk, 0, 0);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, kD, 0, 1);
@@ -51,7 +55,7 @@ struct __align__(1024) Smem {
   uint64_t q_full;
   uint64_t k_full[kKStages], k_empty[kKStages];
   uint64_t v_full[kVStages], v_empty[kVStages];
-  uint64_t s_full[2], p_full[2], pv_done[2], o_full[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_full[2], drain[2];
   int blocks[kMaxSel];
   int n_sel;
   uint32_t tmem_base;
@@ -107,8 +111,7 @@ __device__ __forceinline__ void raise_abort(Smem& s, int* status, int code) {
   if (status) atomicExch(status, code);
 }
 
-// 10 warps: three of them share one SM sub-partition's 16K-entry register file, which caps
-// a thread at 168 registers.
+// 11 warps; a thread fits in 168 registers without spilling.
 __global__ void __launch_bounds__(kThreads, 1)
 sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
@@ -141,6 +144,7 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_init(&s.p_full[i], 4);
       ptx::mbar_init(&s.pv_done[i], 1);
       ptx::mbar_init(&s.o_full[i], 1);
+      ptx::mbar_init(&s.drain[i], 1);
     }
     s.abort = 0;
     ptx::fence_barrier_init();
@@ -220,92 +224,62 @@ sparse_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int j = v_issued > kVStages ? v_issued - kVStages : 0; j < v_issued; ++j)
         ptx::mbar_wait_timed(&s.v_full[j % kVStages], (j / kVStages) & 1);
     }
-  } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------ MMA issuers: warp 9 every Q.K^T, warp 10 every P.V
+    const bool is_qk = warp == kMmaWarp;
     bool ok = true;
     bool issued_any = false;
-    const uint32_t q0 = ptx::smem_u32(s.q[0]), q1 = ptx::smem_u32(s.q[1]);
-    auto issue_qk = [&](int i, int j) {
-      const uint32_t qa = i == 0 ? q0 : q1;
-      const uint32_t kb = ptx::smem_u32(s.k[j % kKStages]);
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * (kTileRows * kRowBytes) + (kk & 3) * 32;
-        ptx::umma_bf16_ss(tmem + i * 128, ptx::smem_desc_k_sw128(qa + off),
-                          ptx::smem_desc_k_sw128(kb + off), kIdescQK, kk > 0 ? 1u : 0u);
-      }
-    };
-    auto issue_pv = [&](int i, int j) {
-      const uint32_t vb = ptx::smem_u32(s.v[j % kVStages]);
-#pragma unroll
-      for (int kk = 0; kk < kBk / 16; ++kk)
-        ptx::umma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
-                          ptx::smem_desc_mn_sw128(vb + kk * 16 * kRowBytes, kBk * kRowBytes, 1024),
-                          kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-    };
-    if (n_sel > 0) {
-      ok = ptx::mbar_wait(&s.q_full, 0, abort) && ptx::mbar_wait(&s.k_full[0], 0, abort);
-      if (ok) {
-        ptx::tc_fence_after_sync();
-        if (lane == 0) {
-          issue_qk(0, 0);
-          ptx::umma_commit(&s.s_full[0]);
-          issue_qk(1, 0);
-          ptx::umma_commit(&s.s_full[1]);
-          ptx::umma_commit(&s.k_empty[0]);
-        }
-        issued_any = true;
-        __syncwarp();
-      }
-      // Q.K^T of the next block overwrites S/P of a Q tile, which the P.V of the previous
-      // block reads from TMEM: it is issued only after that P.V has completed.
+    if (n_sel > 0 && is_qk) {
+      ok = ptx::mbar_wait(&s.q_full, 0, abort);
       for (int j = 0; ok && j < n_sel; ++j) {
-        const bool more = j + 1 < n_sel;
-        if (!ptx::mbar_wait(&s.v_full[j % kVStages], (j / kVStages) & 1, abort) ||
-            !ptx::mbar_wait(&s.p_full[0], j & 1, abort)) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-        if (lane == 0) {
-          issue_pv(0, j);
-          ptx::umma_commit(&s.pv_done[0]);
-          if (!more) ptx::umma_commit(&s.o_full[0]);   // tile 0's epilogue overlaps the last P.V of tile 1
-        }
-        __syncwarp();
-        if (more) {
-          if (!ptx::mbar_wait(&s.k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1, abort) ||
-              !ptx::mbar_wait(&s.pv_done[0], j & 1, abort)) { ok = false; break; }
+        if (!ptx::mbar_wait(&s.k_full[j % kKStages], (j / kKStages) & 1, abort)) { ok = false; break; }
+        for (int i = 0; i < 2; ++i) {
+          // Q.K^T of block j overwrites S/P of tile i, which block j-1's P.V reads
+          if (j > 0 && !ptx::mbar_wait(&s.pv_done[i], (j - 1) & 1, abort)) { ok = false; break; }
           ptx::tc_fence_after_sync();
           if (lane == 0) {
-            issue_qk(0, j + 1);
-            ptx::umma_commit(&s.s_full[0]);
+            const uint32_t qa = ptx::smem_u32(s.q[i]);
+            const uint32_t kb = ptx::smem_u32(s.k[j % kKStages]);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * (kTileRows * kRowBytes) + (kk & 3) * 32;
+              ptx::umma_bf16_ss(tmem + i * 128, ptx::smem_desc_k_sw128(qa + off),
+                                ptx::smem_desc_k_sw128(kb + off), kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            ptx::umma_commit(&s.s_full[i]);
+            if (i == 1) ptx::umma_commit(&s.k_empty[j % kKStages]);
           }
+          issued_any = true;
           __syncwarp();
         }
-        if (!ptx::mbar_wait(&s.p_full[1], j & 1, abort)) { ok = false; break; }
-        ptx::tc_fence_after_sync();
-        if (lane == 0) {
-          issue_pv(1, j);
-          ptx::umma_commit(&s.pv_done[1]);
-          ptx::umma_commit(&s.v_empty[j % kVStages]);
-          if (!more) ptx::umma_commit(&s.o_full[1]);
-        }
-        __syncwarp();
-        if (more) {
-          if (!ptx::mbar_wait(&s.pv_done[1], j & 1, abort)) { ok = false; break; }
+      }
+    } else if (n_sel > 0) {
+      for (int j = 0; ok && j < n_sel; ++j) {
+        if (!ptx::mbar_wait(&s.v_full[j % kVStages], (j / kVStages) & 1, abort)) { ok = false; break; }
+        for (int i = 0; i < 2; ++i) {
+          if (!ptx::mbar_wait(&s.p_full[i], j & 1, abort)) { ok = false; break; }
           ptx::tc_fence_after_sync();
           if (lane == 0) {
-            issue_qk(1, j + 1);
-            ptx::umma_commit(&s.s_full[1]);
-            ptx::umma_commit(&s.k_empty[(j + 1) % kKStages]);
+            const uint32_t vb = ptx::smem_u32(s.v[j % kVStages]);
+#pragma unroll
+            for (int kk = 0; kk < kBk / 16; ++kk)
+              ptx::umma_bf16_ts(tmem + 256 + i * 128, tmem + i * 128 + kk * 8,
+                                ptx::smem_desc_mn_sw128(vb + kk * 16 * kRowBytes, kBk * kRowBytes, 1024),
+                                kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::umma_commit(&s.pv_done[i]);
+            if (i == 1) ptx::umma_commit(&s.v_empty[j % kVStages]);
+            if (j + 1 == n_sel) ptx::umma_commit(&s.o_full[i]);
           }
+          issued_any = true;
           __syncwarp();
         }
       }
     }
     if (!ok && lane == 0) raise_abort(s, status, 0x202);
     if (*abort && lane == 0 && issued_any) {
-      // drain: one more commit covers every MMA issued so far
-      ptx::umma_commit(&s.o_full[0]);
-      ptx::mbar_wait_timed(&s.o_full[0], 0);
+      // drain: one more commit covers every MMA this thread issued
+      ptx::umma_commit(&s.drain[is_qk ? 0 : 1]);
+      ptx::mbar_wait_timed(&s.drain[is_qk ? 0 : 1], 0);
     }
   } else {
     // ------------------------------------------------ softmax + epilogue (warps 0-7)
