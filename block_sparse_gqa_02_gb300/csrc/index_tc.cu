@@ -13,7 +13,10 @@
 // CTA = one (sequence, query tile), heaviest tiles launched first.  Warps:
 //   0-7  epilogue (warp w reads TMEM lanes 32*(w%4)..+31 of accumulator half w/4),
 //   8    TMA producer (query tile once, then key blocks through a 4-stage ring),
-//   9    MMA issuer (one thread), double-buffered accumulators (2 x 256 TMEM columns).
+//   9, 10 MMA issuers (one thread each: rows 0-127 and rows 128-255 of the tile), into
+//        double-buffered accumulators (2 x 256 TMEM columns).  One thread's stream of
+//        N = 128 MMAs with commits in it keeps the tensor core busy only ~60 % of the time;
+//        two interleaved streams fill it.
 // Shared memory operands use the 128-byte swizzle written by TMA; every wait is bounded.
 #include "common.cuh"
 #include "index_tc.cuh"
@@ -34,7 +37,7 @@ constexpr int kRowBytes = 128;     // one swizzled row: 64 bf16
 constexpr int kABytes = 2 * kRows * kRowBytes;   // [chunk][256 rows][128 B] = 64 KiB
 constexpr int kBBytes = 2 * kBk * kRowBytes;     // [chunk][128 rows][128 B] = 32 KiB
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (kEpiWarps + 2) * 32;
+constexpr int kThreads = (kEpiWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, kBk);
 constexpr int kMaxWant = 255;      // fused top-k: up to 255 blocks besides the current one
@@ -43,7 +46,7 @@ struct __align__(1024) Smem {
   uint8_t a[kABytes];
   uint8_t b[kStages][kBBytes];
   uint64_t full[kStages], empty[kStages];
-  uint64_t a_full, acc_full[2], acc_empty[2];
+  uint64_t a_full, acc_full[2], acc_empty[2], drain[2];
   uint64_t pair_bar[kEpiWarps / 2][2];
   float part[2][kEpiWarps];
   // fused top-k: per head, the best blocks seen so far (unordered) and how many
@@ -75,11 +78,12 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       ptx::mbar_init(&s.full[i], 1);
-      ptx::mbar_init(&s.empty[i], 1);
+      ptx::mbar_init(&s.empty[i], 2);          // both issuers' MMAs read the stage
     }
     ptx::mbar_init(&s.a_full, 1);
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&s.acc_full[i], 1);
+      ptx::mbar_init(&s.acc_full[i], 2);       // both halves of the accumulator
+      ptx::mbar_init(&s.drain[i], 1);
       ptx::mbar_init(&s.acc_empty[i], kEpiWarps);
     }
     for (int i = 0; i < kEpiWarps / 2; ++i) {
@@ -141,8 +145,9 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
         ptx::mbar_wait_timed(&s.full[i % kStages], (i / kStages) & 1);
     }
-  } else if (warp == kEpiWarps + 1) {
-    // -------------------------------------------------------------- MMA issuer
+  } else if (warp == kEpiWarps + 1 || warp == kEpiWarps + 2) {
+    // ------------------------------------------------ MMA issuers, one per 128 rows
+    const int h = warp - (kEpiWarps + 1);
     int issued = 0;
     bool ok = ptx::mbar_wait(&s.a_full, 0, abort);
     for (int i = 0; ok && i < nblk; ++i) {
@@ -159,17 +164,15 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) {
         const uint32_t a0 = ptx::smem_u32(s.a), b0 = ptx::smem_u32(s.b[st]);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int kk = 0; kk < kDI / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * (kRows * kRowBytes) + (kk & 3) * 32;
-            const uint32_t kb = (kk >> 2) * (kBk * kRowBytes) + (kk & 3) * 32;
-            ptx::umma_bf16_ss(tmem + buf * 256 + h * 128,
-                              ptx::smem_desc_k_sw128(a0 + ka + h * 128 * kRowBytes),
-                              ptx::smem_desc_k_sw128(b0 + kb), kIdesc, kk > 0 ? 1u : 0u);
-          }
-        ptx::umma_commit(&s.empty[st]);      // stage reusable once these MMAs finish
-        ptx::umma_commit(&s.acc_full[buf]);  // accumulator ready for the epilogue
+        for (int kk = 0; kk < kDI / 16; ++kk) {
+          const uint32_t ka = (kk >> 2) * (kRows * kRowBytes) + (kk & 3) * 32;
+          const uint32_t kb = (kk >> 2) * (kBk * kRowBytes) + (kk & 3) * 32;
+          ptx::umma_bf16_ss(tmem + buf * 256 + h * 128,
+                            ptx::smem_desc_k_sw128(a0 + ka + h * 128 * kRowBytes),
+                            ptx::smem_desc_k_sw128(b0 + kb), kIdesc, kk > 0 ? 1u : 0u);
+        }
+        ptx::umma_commit(&s.empty[st]);      // stage reusable once both halves' MMAs finish
+        ptx::umma_commit(&s.acc_full[buf]);  // accumulator ready once both halves are done
       }
       issued = i + 1;
       __syncwarp();
@@ -178,8 +181,10 @@ index_scores_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) raise_abort(s, status, 0x102);
     }
     if (*abort && lane == 0 && issued > 0) {
-      // the tensor core must be done with TMEM and shared memory before teardown
-      ptx::mbar_wait_timed(&s.acc_full[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+      // the tensor core must be done with TMEM and shared memory before teardown: one more
+      // commit covers every MMA this thread issued
+      ptx::umma_commit(&s.drain[h]);
+      ptx::mbar_wait_timed(&s.drain[h], 0);
     }
   } else {
     // ---------------------------------------------------------------- epilogue

@@ -22,7 +22,9 @@
 //   in TMEM over all of the CTA's groups.  A CTA adds its dK / dV to the fp32 outputs with
 //   vector atomics (a heavily selected block is split over several CTAs).
 // Warps: 8 elementwise warps (two per TMEM lane quadrant, each taking half of the columns of
-// S / dP or S^T / dP^T), a TMA producer and an MMA issuer.  Every wait is bounded.
+// S / dP or S^T / dP^T), a TMA producer and two MMA issuers (a single thread's stream of
+// N = 128 MMAs with commits in it keeps the tensor core busy only ~60 % of the time).  Every
+// wait is bounded.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sparse_backward_tc.cuh"
@@ -39,8 +41,8 @@ constexpr int kRows = 128;                              // rows of one Q group
 constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;       // [2 chunks][128 rows][128 B] = 32 KiB
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 320;                           // 8 math warps, producer, MMA issuer
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 352;                           // 8 math warps, producer, 2 MMA issuers
+constexpr int kProducerWarp = 8, kMmaWarp = 9;       // MMA issuers: warps 9 and 10
 constexpr int kMathWarps = 8;                           // two per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);   // both operands K-major
@@ -118,7 +120,7 @@ struct __align__(1024) SmemQ {
   uint8_t v[2][kTileBytes];
   uint64_t qd_full;
   uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full, s_free, ds_full, dq_done, drain;
+  uint64_t s_full, s_free, ds_full, dq_done, drain[2];
   int blocks[kMaxSel];
   int n_sel;
   uint32_t tmem_base;
@@ -155,7 +157,8 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     ptx::mbar_init(&s.s_free, kMathWarps);
     ptx::mbar_init(&s.ds_full, kMathWarps);
     ptx::mbar_init(&s.dq_done, 1);
-    ptx::mbar_init(&s.drain, 1);
+    ptx::mbar_init(&s.drain[0], 1);
+    ptx::mbar_init(&s.drain[1], 1);
     s.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -222,49 +225,49 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
         ptx::mbar_wait_timed(&s.kv_full[j & 1], (j >> 1) & 1);
     }
-  } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------- MMA issuers
+    // warp 9: S = Q K^T and dP = dO V^T of each block (into TMEM once the math warps have
+    // read the previous block's); warp 10: dQ += dS K once the math warps have written dS.
+    // One thread's stream of N = 128 MMAs with commits keeps the tensor core busy only
+    // ~60 % of the time; two streams fill it.
+    const int who = warp - kMmaWarp;
     bool ok = true, issued_any = false;
     const uint32_t qa = ptx::smem_u32(s.q), da = ptx::smem_u32(s.dO);
-    if (n_sel > 0) {
-      ok = ptx::mbar_wait(&s.qd_full, 0, abort) && ptx::mbar_wait(&s.kv_full[0], 0, abort);
-      if (ok) {
+    if (n_sel > 0 && who == 0) {
+      ok = ptx::mbar_wait(&s.qd_full, 0, abort);
+      for (int j = 0; ok && j < n_sel; ++j) {
+        // S / dP of block j once the math warps have read block j-1's
+        if (!ptx::mbar_wait(&s.kv_full[j & 1], (j >> 1) & 1, abort) ||
+            (j > 0 && !ptx::mbar_wait(&s.s_free, (j - 1) & 1, abort))) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
-          mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[0]));
-          mma_kk(tmem + kColDP, da, ptx::smem_u32(s.v[0]));
+          mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[j & 1]));
+          mma_kk(tmem + kColDP, da, ptx::smem_u32(s.v[j & 1]));
           ptx::umma_commit(&s.s_full);
         }
         issued_any = true;
         __syncwarp();
       }
+    } else if (n_sel > 0) {
       for (int j = 0; ok && j < n_sel; ++j) {
-        if (j + 1 < n_sel) {
-          // S / dP of the next block once the math warps have read this block's
-          if (!ptx::mbar_wait(&s.kv_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort) ||
-              !ptx::mbar_wait(&s.s_free, j & 1, abort)) { ok = false; break; }
-          ptx::tc_fence_after_sync();
-          if (lane == 0) {
-            mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[(j + 1) & 1]));
-            mma_kk(tmem + kColDP, da, ptx::smem_u32(s.v[(j + 1) & 1]));
-            ptx::umma_commit(&s.s_full);
-          }
-          __syncwarp();
-        }
         if (!ptx::mbar_wait(&s.ds_full, j & 1, abort)) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
           mma_tmn(tmem + kColDQ, tmem + kColDS, ptx::smem_u32(s.k[j & 1]), j > 0);
           ptx::umma_commit(&s.dq_done);
+          // block j's K and V are free: its S and dP completed before the math warps
+          // formed dS, and this dQ product was the last to read K
           ptx::umma_commit(&s.kv_empty[j & 1]);
         }
+        issued_any = true;
         __syncwarp();
       }
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x502);
     if (*abort && lane == 0 && issued_any) {
-      ptx::umma_commit(&s.drain);                          // covers every MMA issued so far
-      ptx::mbar_wait_timed(&s.drain, 0);
+      ptx::umma_commit(&s.drain[who]);                     // covers this thread's MMAs
+      ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
     // ------------------------- math warps 0-7: warp w takes row quadrant w % 4 and the key
@@ -389,7 +392,7 @@ struct __align__(1024) SmemKV {
   uint8_t dO[2][kTileBytes];
   float rec[2][2 * kRows];       // a group's lse2 [0,128) and D [128,256), per stage
   uint64_t kv_full, g_full[2], g_empty[2];
-  uint64_t s_full, p_full, acc_done, drain;
+  uint64_t s_full, p_full, acc_dk, acc_dv, drain[2];
   int tiles[kMaxTilesPerCta];
   int n_tiles;
   uint32_t tmem_base;
@@ -446,12 +449,14 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     ptx::mbar_init(&s.kv_full, 1);
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s.g_full[i], 1);
-      ptx::mbar_init(&s.g_empty[i], 1);
+      ptx::mbar_init(&s.g_empty[i], 2);   // both issuers' MMAs read the group
     }
-    ptx::mbar_init(&s.s_full, 1);
+    ptx::mbar_init(&s.s_full, 2);           // S^T from one issuer, dP^T from the other
     ptx::mbar_init(&s.p_full, kMathWarps);
-    ptx::mbar_init(&s.acc_done, 1);
-    ptx::mbar_init(&s.drain, 1);
+    ptx::mbar_init(&s.acc_dk, 1);
+    ptx::mbar_init(&s.acc_dv, 1);
+    ptx::mbar_init(&s.drain[0], 1);
+    ptx::mbar_init(&s.drain[1], 1);
     s.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -505,19 +510,25 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int gi = issued > 2 ? issued - 2 : 0; gi < issued; ++gi)
         ptx::mbar_wait_timed(&s.g_full[gi & 1], (gi >> 1) & 1);
     }
-  } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ------------------------------------------------------------- MMA issuers
+    // warp 9: S^T = K Q^T, then dK += dS^T Q; warp 10: dP^T = V dO^T, then dV += P^T dO.
+    // P^T is written over S^T and read by dV, dS^T over dP^T and read by dK, so each
+    // issuer's next product waits for the other issuer's last one, never for its own.
+    const int who = warp - kMmaWarp;
     bool ok = ptx::mbar_wait(&s.kv_full, 0, abort);
     bool issued_any = false;
     const uint32_t ka = ptx::smem_u32(s.k), va = ptx::smem_u32(s.v);
+    uint64_t* my_acc = who == 0 ? &s.acc_dk : &s.acc_dv;
+    uint64_t* other_acc = who == 0 ? &s.acc_dv : &s.acc_dk;
     for (int gi = 0; ok && gi < n_groups; ++gi) {
       const int st = gi & 1;
       if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
-          (gi > 0 && !ptx::mbar_wait(&s.acc_done, (gi - 1) & 1, abort))) { ok = false; break; }
+          (gi > 0 && !ptx::mbar_wait(other_acc, (gi - 1) & 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
       if (lane == 0) {
-        mma_kk(tmem + kColS, ka, ptx::smem_u32(s.q[st]));
-        mma_kk(tmem + kColDP, va, ptx::smem_u32(s.dO[st]));
+        if (who == 0) mma_kk(tmem + kColS, ka, ptx::smem_u32(s.q[st]));
+        else mma_kk(tmem + kColDP, va, ptx::smem_u32(s.dO[st]));
         ptx::umma_commit(&s.s_full);
       }
       issued_any = true;
@@ -525,17 +536,17 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ptx::mbar_wait(&s.p_full, gi & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       if (lane == 0) {
-        mma_tmn(tmem + kColDV, tmem + kColS, ptx::smem_u32(s.dO[st]), gi > 0, true);
-        mma_tmn(tmem + kColDK, tmem + kColDP, ptx::smem_u32(s.q[st]), gi > 0, true);
-        ptx::umma_commit(&s.acc_done);
+        if (who == 0) mma_tmn(tmem + kColDK, tmem + kColDP, ptx::smem_u32(s.q[st]), gi > 0, true);
+        else mma_tmn(tmem + kColDV, tmem + kColS, ptx::smem_u32(s.dO[st]), gi > 0, true);
+        ptx::umma_commit(my_acc);
         ptx::umma_commit(&s.g_empty[st]);
       }
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x602);
     if (*abort && lane == 0 && issued_any) {
-      ptx::umma_commit(&s.drain);                          // covers every MMA issued so far
-      ptx::mbar_wait_timed(&s.drain, 0);
+      ptx::umma_commit(&s.drain[who]);                     // covers this thread's MMAs
+      ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
     // ----------------- math warps 0-7: one key of the block per lane (quadrant w % 4); warp
@@ -589,7 +600,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (lane == 0) ptx::mbar_arrive(&s.p_full);
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x603);
-    bool have = ok && ptx::mbar_wait(&s.acc_done, (n_groups - 1) & 1, abort);
+    bool have = ok && ptx::mbar_wait(&s.acc_dk, (n_groups - 1) & 1, abort) &&
+                ptx::mbar_wait(&s.acc_dv, (n_groups - 1) & 1, abort);
     if (ok && !have && lane == 0) raise_abort(&s.abort, status, 0x604);
     if (have) {
       ptx::tc_fence_after_sync();
