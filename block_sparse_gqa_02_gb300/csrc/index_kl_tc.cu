@@ -23,7 +23,8 @@
 //   token's G rows are adjacent columns; gz^T goes to TMEM and d idx_k += gz^T idx_q
 //   accumulates there over all of the CTA's groups before one set of vector atomics.
 // Warps: 8 elementwise warps (two per TMEM lane quadrant, each taking half of the columns),
-// a TMA producer and an MMA issuer.  Every wait is bounded.
+// a TMA producer and two MMA issuers (a single thread's stream of N = 128 MMAs with commits
+// in it keeps the tensor core busy only ~60 % of the time).  Every wait is bounded.
 #include "common.cuh"
 #include "index_kl_tc.cuh"
 #include "ptx.cuh"
@@ -41,8 +42,8 @@ constexpr int kRows = 128;
 constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;           // [2 chunks][128 rows][128 B]
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 320;                               // 8 math warps, producer, MMA
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 352;                               // 8 math warps, producer, 2 MMA
+constexpr int kProducerWarp = 8, kMmaWarp = 9;             // MMA issuers: warps 9, 10
 constexpr int kMathWarps = 8;                               // two per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);
@@ -95,7 +96,7 @@ struct __align__(1024) SmemR {
   uint8_t ik[2][kTileBytes];
   uint64_t q_full, ring_full[2], ring_empty[2];
   uint64_t z_full[2], z_free[2], pass1_done;
-  uint64_t s_full, g_full, dq_done, drain;
+  uint64_t s_full, g_full, dq_done, drain[2];
   float half_ml[2][2][kRows];   // pass 1: [column half][max, sum][row]
   int blocks[kMaxSel];
   int n_sel;
@@ -133,7 +134,8 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     ptx::mbar_init(&s.s_full, 1);
     ptx::mbar_init(&s.g_full, kMathWarps);
     ptx::mbar_init(&s.dq_done, 1);
-    ptx::mbar_init(&s.drain, 1);
+    ptx::mbar_init(&s.drain[0], 1);
+    ptx::mbar_init(&s.drain[1], 1);
     s.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -213,55 +215,68 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int rr = issued > 2 ? issued - 2 : 0; rr < issued; ++rr)
         ptx::mbar_wait_timed(&s.ring_full[rr & 1], (rr >> 1) & 1);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // warp 9: pass 1's Z and pass 2's S and Z; warp 10: pass 2's dIQ += gz idx_k (a single
+    // thread's stream of N = 128 MMAs with commits keeps the tensor core busy only ~60 %
+    // of the time).  S and Z of block j overwrite the gz of block j-1, so they wait for
+    // warp 10's product of block j-1.
+    const int who = warp - kMmaWarp;
     bool ok = true, issued_any = false;
     const uint32_t qa = ptx::smem_u32(s.q), za = ptx::smem_u32(s.iqr);
-    for (int j = 0; ok && j < n_sel; ++j) {                  // pass 1
-      const int st = j & 1, buf = j & 1;
-      if (!ptx::mbar_wait(&s.ring_full[st], (j >> 1) & 1, abort) ||
-          !ptx::mbar_wait(&s.z_free[buf], ((j >> 1) & 1) ^ 1, abort)) { ok = false; break; }
-      ptx::tc_fence_after_sync();
-      if (lane == 0) {
-        mma_kk(tmem + buf * 128, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
-        ptx::umma_commit(&s.z_full[buf]);
-        ptx::umma_commit(&s.ring_empty[st]);
+    if (who == 0) {
+      for (int j = 0; ok && j < n_sel; ++j) {                // pass 1
+        const int st = j & 1, buf = j & 1;
+        if (!ptx::mbar_wait(&s.ring_full[st], (j >> 1) & 1, abort) ||
+            !ptx::mbar_wait(&s.z_free[buf], ((j >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          mma_kk(tmem + buf * 128, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
+          ptx::umma_commit(&s.z_full[buf]);
+          ptx::umma_commit(&s.ring_empty[st]);
+        }
+        issued_any = true;
+        __syncwarp();
       }
-      issued_any = true;
-      __syncwarp();
-    }
-    if (ok && n_sel > 0)
-      ok = ptx::mbar_wait(&s.pass1_done, 0, abort) && ptx::mbar_wait(&s.q_full, 0, abort);
-    for (int j = 0; ok && j < n_sel; ++j) {                  // pass 2
-      const int rr = n_sel + j, st = rr & 1;
-      if (!ptx::mbar_wait(&s.ring_full[st], (rr >> 1) & 1, abort) ||
-          (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort))) { ok = false; break; }
-      ptx::tc_fence_after_sync();
-      if (lane == 0) {
-        mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[st]), kBk * kRowBytes, kIdescKK);
-        mma_kk(tmem + kColZ, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
-        ptx::umma_commit(&s.s_full);
+      if (ok && n_sel > 0)
+        ok = ptx::mbar_wait(&s.pass1_done, 0, abort) && ptx::mbar_wait(&s.q_full, 0, abort);
+      for (int j = 0; ok && j < n_sel; ++j) {                // pass 2: S and Z
+        const int rr = n_sel + j, st = rr & 1;
+        if (!ptx::mbar_wait(&s.ring_full[st], (rr >> 1) & 1, abort) ||
+            (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort))) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[st]), kBk * kRowBytes, kIdescKK);
+          mma_kk(tmem + kColZ, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
+          ptx::umma_commit(&s.s_full);
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      if (!ptx::mbar_wait(&s.g_full, j & 1, abort)) { ok = false; break; }
-      ptx::tc_fence_after_sync();
-      if (lane == 0) {
-        // dIQ += gz idx_k: gz (rows x keys) from TMEM (keys 64-127 at columns 96-127),
-        // idx_k as the MN-major B operand
+    } else {
+      for (int j = 0; ok && j < n_sel; ++j) {                // pass 2: dIQ += gz idx_k
+        const int rr = n_sel + j, st = rr & 1;
+        if (!ptx::mbar_wait(&s.g_full, j & 1, abort)) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          // gz (rows x keys) from TMEM (keys 64-127 at columns 96-127), idx_k as the
+          // MN-major B operand; block j's ring stage is free once this product finishes
+          // (its S and Z completed before the math warps formed gz)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::umma_bf16_ts(tmem + kColDQ, tmem + kColS + kk * 8 + (kk >= 4 ? 64 : 0),
-                            ptx::smem_desc_mn_sw128(ptx::smem_u32(s.ik[st]) + kk * 16 * kRowBytes,
-                                                    kBk * kRowBytes, 1024),
-                            kIdescMN, (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::umma_commit(&s.dq_done);
-        ptx::umma_commit(&s.ring_empty[st]);
+          for (int kk = 0; kk < 8; ++kk)
+            ptx::umma_bf16_ts(tmem + kColDQ, tmem + kColS + kk * 8 + (kk >= 4 ? 64 : 0),
+                              ptx::smem_desc_mn_sw128(ptx::smem_u32(s.ik[st]) + kk * 16 * kRowBytes,
+                                                      kBk * kRowBytes, 1024),
+                              kIdescMN, (j > 0 || kk > 0) ? 1u : 0u);
+          ptx::umma_commit(&s.dq_done);
+          ptx::umma_commit(&s.ring_empty[st]);
+        }
+        issued_any = true;
+        __syncwarp();
       }
-      __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x702);
     if (*abort && lane == 0 && issued_any) {
-      ptx::umma_commit(&s.drain);
-      ptx::mbar_wait_timed(&s.drain, 0);
+      ptx::umma_commit(&s.drain[who]);
+      ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
     // ------------------------- math warps 0-7: warp w takes row quadrant w % 4 and the key
@@ -273,8 +288,10 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     bool ok = true;
-    // pass 1: log2-sum-exp of the index logits over the tile's visible keys (this warp's
-    // half of the columns, then combined with the other half's)
+    // pass 1: log2-sum-exp of the index logits over the tile's visible keys.  The G rows
+    // (lanes) of a token hold the same index logits, so lane hh takes keys hh, hh + G, ...
+    // of this warp's half of the columns; the token's lanes, then the two halves, are
+    // combined at the end.
     float mI = -INFINITY, lI = 0.f;
     for (int j = 0; j < n_sel; ++j) {
       const int buf = j & 1, lim = t - s.blocks[j] * kBk;
@@ -291,19 +308,36 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int c = 2 * half + u;
+        float zk[32 / G];                                    // this lane's keys of the chunk
         float cm = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          if (c * 32 + e <= lim) cm = fmaxf(cm, __uint_as_float(zv[u][e]) * c2);
+        for (int i = 0; i < 32 / G; ++i) {
+          float z = __uint_as_float(zv[u][i * G]);
+#pragma unroll
+          for (int x = 1; x < G; ++x)
+            if (hh == x) z = __uint_as_float(zv[u][i * G + x]);
+          zk[i] = c * 32 + i * G + hh <= lim ? z * c2 : -INFINITY;
+          cm = fmaxf(cm, zk[i]);
+        }
         if (cm != -INFINITY) {
           const float mn = fmaxf(mI, cm);
           float acc = 0.f;
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (c * 32 + e <= lim) acc += ex2(fmaf(__uint_as_float(zv[u][e]), c2, -mn));
+          for (int i = 0; i < 32 / G; ++i) acc += ex2(zk[i] - mn);
           lI = lI * ex2(mI - mn) + acc;
           mI = mn;
         }
+      }
+    }
+    // combine the token's G lanes
+#pragma unroll
+    for (int o = 1; o < G; o <<= 1) {
+      const float mo = __shfl_xor_sync(0xffffffffu, mI, o);
+      const float lo = __shfl_xor_sync(0xffffffffu, lI, o);
+      const float mn = fmaxf(mI, mo);
+      if (mn != -INFINITY) {
+        lI = lI * ex2(mI - mn) + lo * ex2(mo - mn);
+        mI = mn;
       }
     }
     // every math warp reaches this barrier exactly once (also after a failed wait)
@@ -446,7 +480,7 @@ struct __align__(1024) SmemK {
   uint8_t iq[2][kIqBytes];
   float rec[2][2 * kRows];     // a group's lse2 per row [0,128), lseI2 per token [128,..)
   uint64_t kv_full, g_full[2], g_empty[2];
-  uint64_t s_full, p_full, acc_done, drain;
+  uint64_t s_full[2], p_full[2], acc_done[2], drain[2];   // per S^T / gz^T buffer
   int tiles[kMaxTilesPerCta];
   int n_tiles;
   uint32_t tmem_base;
@@ -505,10 +539,12 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_init(&s.g_full[i], 1);
       ptx::mbar_init(&s.g_empty[i], 1);
     }
-    ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.p_full, kMathWarps);
-    ptx::mbar_init(&s.acc_done, 1);
-    ptx::mbar_init(&s.drain, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.s_full[i], 1);
+      ptx::mbar_init(&s.p_full[i], kMathWarps);
+      ptx::mbar_init(&s.acc_done[i], 1);
+      ptx::mbar_init(&s.drain[i], 1);
+    }
     s.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -521,9 +557,16 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   ptx::tc_fence_after_sync();
   const uint32_t tmem = s.tmem_base;
-  // TMEM: S^T [0,128) (keys x rows), Z^T [128,128+kNTok) (keys x tokens), gz^T bf16
-  // [192,224), dIK [256,384) (keys x index dims)
-  constexpr uint32_t kColS = 0, kColZ = 128, kColG = 192, kColDK = 256;
+  // TMEM: S^T (keys x rows, 128 columns), Z^T (keys x tokens, kNTok), gz^T (bf16, kNTok / 2),
+  // dIK [256,384) (keys x index dims).  With at most 32 tokens a group (G >= 4) the first
+  // three are double-buffered -- S^T at 0 and 384, Z^T at 128 and 160, gz^T at 192 and 224 --
+  // so the next group's S^T and Z^T are computed while the math warps work on this group;
+  // with 64 (G = 2) they are single: S^T 0, Z^T [128,192), gz^T [192,224).
+  constexpr int kNBuf = kNTok <= 32 ? 2 : 1;
+  constexpr uint32_t kColDK = 256;
+  auto col_s = [](int b) -> uint32_t { return b == 0 ? 0u : 384u; };
+  auto col_z = [](int b) -> uint32_t { return b == 0 ? 128u : 160u; };
+  auto col_g = [](int b) -> uint32_t { return b == 0 ? 192u : 224u; };
   constexpr uint32_t kIdescZ = ptx::idesc_bf16_f32(128, kNTok, 0, 0);
 
   if (warp == kProducerWarp) {
@@ -561,40 +604,48 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int gi = issued > 2 ? issued - 2 : 0; gi < issued; ++gi)
         ptx::mbar_wait_timed(&s.g_full[gi & 1], (gi >> 1) & 1);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // warp 9: S^T and Z^T of each group (after the math warps released the previous
+    // group's); warp 10: dIK += gz^T idx_q
+    const int who = warp - kMmaWarp;
     bool ok = ptx::mbar_wait(&s.kv_full, 0, abort);
     bool issued_any = false;
     const uint32_t ka = ptx::smem_u32(s.k), ia = ptx::smem_u32(s.ik);
     for (int gi = 0; ok && gi < n_groups; ++gi) {
-      const int st = gi & 1;
-      if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort)) { ok = false; break; }
-      ptx::tc_fence_after_sync();
-      if (lane == 0) {
-        mma_kk(tmem + kColS, ka, ptx::smem_u32(s.q[st]), kRows * kRowBytes, kIdescKK);
-        mma_kk(tmem + kColZ, ia, ptx::smem_u32(s.iq[st]), kIqRows * kRowBytes, kIdescZ);
-        ptx::umma_commit(&s.s_full);
+      const int st = gi & 1, bf = gi % kNBuf;
+      const uint32_t ph = (gi / kNBuf) & 1;
+      if (who == 0) {
+        // S^T and Z^T of group gi, into a buffer the math warps have finished with
+        if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
+            (gi >= kNBuf && !ptx::mbar_wait(&s.p_full[bf], ph ^ 1, abort))) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          mma_kk(tmem + col_s(bf), ka, ptx::smem_u32(s.q[st]), kRows * kRowBytes, kIdescKK);
+          mma_kk(tmem + col_z(bf), ia, ptx::smem_u32(s.iq[st]), kIqRows * kRowBytes, kIdescZ);
+          ptx::umma_commit(&s.s_full[bf]);
+        }
+      } else {
+        if (!ptx::mbar_wait(&s.p_full[bf], ph, abort)) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        if (lane == 0) {
+          // dIK += gz^T (keys x tokens, TMEM) idx_q (tokens x index dims, MN-major B)
+#pragma unroll
+          for (int kk = 0; kk < kNTok / 16; ++kk)
+            ptx::umma_bf16_ts(tmem + kColDK, tmem + col_g(bf) + kk * 8,
+                              ptx::smem_desc_mn_sw128(ptx::smem_u32(s.iq[st]) + kk * 16 * kRowBytes,
+                                                      kIqRows * kRowBytes, 1024),
+                              kIdescMN, (gi > 0 || kk > 0) ? 1u : 0u);
+          ptx::umma_commit(&s.acc_done[bf]);
+          ptx::umma_commit(&s.g_empty[st]);
+        }
       }
       issued_any = true;
-      __syncwarp();
-      if (!ptx::mbar_wait(&s.p_full, gi & 1, abort)) { ok = false; break; }
-      ptx::tc_fence_after_sync();
-      if (lane == 0) {
-        // dIK += gz^T (keys x tokens, TMEM) idx_q (tokens x index dims, MN-major B)
-#pragma unroll
-        for (int kk = 0; kk < kNTok / 16; ++kk)
-          ptx::umma_bf16_ts(tmem + kColDK, tmem + kColG + kk * 8,
-                            ptx::smem_desc_mn_sw128(ptx::smem_u32(s.iq[st]) + kk * 16 * kRowBytes,
-                                                    kIqRows * kRowBytes, 1024),
-                            kIdescMN, (gi > 0 || kk > 0) ? 1u : 0u);
-        ptx::umma_commit(&s.acc_done);
-        ptx::umma_commit(&s.g_empty[st]);
-      }
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x712);
     if (*abort && lane == 0 && issued_any) {
-      ptx::umma_commit(&s.drain);
-      ptx::mbar_wait_timed(&s.drain, 0);
+      ptx::umma_commit(&s.drain[who]);
+      ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
     // ----------------- math warps 0-7: one key of the block per lane (quadrant w % 4); warp
@@ -605,38 +656,36 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int key = blk * kBk + quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
-    if (half == 0 && kHalfTok < 32) {
-      // gz^T columns past the group's tokens (the padding up to the UMMA's 16) stay zero
-      const uint32_t zero[16] = {};
-      for (int c0 = kHalfTok; c0 < 32; c0 += 16) {
-        uint32_t z16[16];
+    if (half == 0 && kTok < 16) {
+      // gz^T columns past the group's tokens (the padding up to the UMMA's K of 16) stay zero
+      uint32_t z8[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) z16[e] = zero[e];
-        ptx::tmem_st_x16(tmem + lane_off + kColG + c0, z16);
-      }
+      for (int e = 0; e < 8; ++e) z8[e] = 0u;
+      for (int bf = 0; bf < kNBuf; ++bf) ptx::tmem_st_x8(tmem + lane_off + col_g(bf), z8);
       ptx::tmem_st_wait();
     }
     bool ok = true;
     for (int gi = 0; gi < n_groups; ++gi) {
-      const int st = gi & 1;
+      const int st = gi & 1, bf = gi % kNBuf;
+      const uint32_t ph = (gi / kNBuf) & 1;
       const int m = s.tiles[gi / parts], part = gi % parts;
       const int t0 = m * kQt + part * kTok;
       if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
-          !ptx::mbar_wait(&s.s_full, gi & 1, abort) ||
-          // the previous group's d idx_k MMA has read gz^T
-          (gi > 0 && !ptx::mbar_wait(&s.acc_done, (gi - 1) & 1, abort))) { ok = false; break; }
+          !ptx::mbar_wait(&s.s_full[bf], ph, abort) ||
+          // the d idx_k MMA of the group that last used this gz^T buffer has read it
+          (gi >= kNBuf && !ptx::mbar_wait(&s.acc_done[bf], ph ^ 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
       uint32_t sv[2][32];
 #pragma unroll
       for (int u = 0; u < 2; ++u)
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + col_s(bf) + (2 * half + u) * 32, sv[u]);
       // this warp's tokens' Z^T columns (loaded 16 at a time; a 16-column load that runs past
       // the Z^T columns reads unused TMEM and those values are not used)
       constexpr int kZLoads = kHalfTok < 16 ? 1 : kHalfTok / 16;
       uint32_t zv[kZLoads][16];
 #pragma unroll
       for (int c = 0; c < kZLoads; ++c)
-        ptx::tmem_ld_x16(tmem + lane_off + kColZ + half * kHalfTok + c * 16, zv[c]);
+        ptx::tmem_ld_x16(tmem + lane_off + col_z(bf) + half * kHalfTok + c * 16, zv[c]);
       ptx::tmem_ld_wait();
       float pt[kHalfTok];
 #pragma unroll
@@ -668,7 +717,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         pk[tk >> 1] = pack_bf16x2(gz2[0], gz2[1]);
       }
       // this warp's tokens' gz^T columns (2 tokens per column)
-      const uint32_t gcol = tmem + lane_off + kColG + half * (kHalfTok / 2);
+      const uint32_t gcol = tmem + lane_off + col_g(bf) + half * (kHalfTok / 2);
       if constexpr (kHalfTok / 2 == 1) ptx::tmem_st_x1(gcol, pk);
       else if constexpr (kHalfTok / 2 == 2) ptx::tmem_st_x2(gcol, pk);
       else if constexpr (kHalfTok / 2 == 4) ptx::tmem_st_x4(gcol, pk);
@@ -677,10 +726,12 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s.p_full);
+      if (lane == 0) ptx::mbar_arrive(&s.p_full[bf]);
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x713);
-    const bool have = ok && ptx::mbar_wait(&s.acc_done, (n_groups - 1) & 1, abort);
+    // the last d idx_k MMA (one issuing thread: it follows all the others)
+    const bool have = ok && ptx::mbar_wait(&s.acc_done[(n_groups - 1) % kNBuf],
+                                           ((n_groups - 1) / kNBuf) & 1, abort);
     if (have) {
       ptx::tc_fence_after_sync();
       const bool in_range = key < p.Sk;
