@@ -42,6 +42,8 @@ LENS = {
     "ragged_long": [1 << 18, 123457, 65536, 3],
     # the scan shares its CTAs out by length: one long cache takes most of them
     "one_long_many_short": [200_000] + [1 + 37 * i for i in range(19)],
+    # more than 2048 blocks in the longest cache (the top-k's long-row form)
+    "past_2048_blocks": [300_000, 64 * 128, 64 * 128 + 1, 0, 4097],
     # more sequences than SMs: the scan falls back to splitting each sequence evenly
     "more_sequences_than_sms": [1 + (97 * i) % 700 for i in range(160)],
 }

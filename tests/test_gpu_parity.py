@@ -115,6 +115,51 @@ def test_topk_1m_prefill_rows_bit_exact():
     assert np.array_equal(got[:, :, rows], ref)
 
 
+@pytest.mark.parametrize("k", [2, 64, 257, 258])
+def test_topk_long_rows_k_bit_exact(k):
+    """Rows of more than 2048 candidates (the 1024-thread form of the kernel) at k = 2,
+    the decode bench's k, and k past 256."""
+    B, L, bs = 2, 3001 * 128 - 5, 128
+    shape = _lib.make_shape(B, 1, L, 64, 4, 128, 128, bs, k, 1, "bf16")
+    sc = random_block_scores((B, 4, 1, shape.n_blocks), seed=20 + k, kind="mixed")
+    sel = torch.full((B, 4, 1, k), -7, dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk(shape, torch.from_numpy(sc).to(DEV), sel)
+    assert np.array_equal(sel.cpu().numpy(), oracle.block_topk_decode(sc, L, bs, k))
+
+
+def test_topk_long_rows_equal_scores_bit_exact():
+    """Every candidate of a row equal (+0 and -0 mixed; a constant), so every digit of the
+    select ties and the lowest block indices are kept."""
+    B, L, bs, k = 2, 2600 * 128, 128, 64
+    shape = _lib.make_shape(B, 1, L, 64, 4, 128, 128, bs, k, 1, "bf16")
+    rng = np.random.default_rng(21)
+    sc = np.where(rng.random((B, 4, 1, shape.n_blocks)) < 0.5, 0.0, -0.0).astype(np.float32)
+    sc[1, 2] = 1.5
+    sc[1, 3, 0, 2000:] = -2.0                   # equal within the row's last quarters
+    sel = torch.full((B, 4, 1, k), -7, dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk(shape, torch.from_numpy(sc).to(DEV), sel)
+    assert np.array_equal(sel.cpu().numpy(), oracle.block_topk_decode(sc, L, bs, k))
+
+
+def test_topk_ragged_long_rows_bit_exact():
+    """Ragged decode rows under a maximum of more than 2048 blocks: empty, shorter than k,
+    exactly k, one past k, and long."""
+    k, bs = 64, 128
+    lens = [0, 1, 63 * bs + 5, 64 * bs, 64 * bs + 1, 66 * bs + 3, 128 * bs, 5000, 2100 * bs,
+            2345 * bs - 17]
+    B = len(lens)
+    shape = _lib.make_shape(B, 1, max(lens), 64, 4, 128, 128, bs, k, 1, "bf16")
+    sc = random_block_scores((B, 4, 1, shape.n_blocks), seed=22, kind="ties")
+    sel = torch.full((B, 4, 1, k), -7, dtype=torch.int32, device=DEV)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    _lib.msa_block_topk_ragged(shape, lens_t, torch.from_numpy(sc).to(DEV), sel)
+    got = sel.cpu().numpy()
+    for b, L in enumerate(lens):
+        ref = (np.full((1, 4, 1, k), -1, dtype=np.int32) if L == 0 else
+               oracle.block_topk_decode(sc[b:b + 1], L, bs, k))
+        assert np.array_equal(got[b:b + 1], ref), f"sequence {b} (length {L})"
+
+
 # -------------------------------------------------------------- index scores
 
 def _index_case(cfg, tiles=None):
