@@ -15,16 +15,21 @@
 // * rows (query-tile order, one CTA per 128 (token, head) rows like the forward): a first
 //   pass over the blocks forms lseI2 from Z = idx_q idx_k^T, with each row's idx_q replicated
 //   so that every row of a token holds its token's index logits; a second pass forms S and Z
-//   again, the math warps average the G rows of a token with warp shuffles, accumulate the
-//   loss and write gz into TMEM, and d idx_q += gz idx_k accumulates in TMEM.  It leaves each
-//   128-row group's main lse2 (per row) and lseI2 (per token) as one 1 KiB record.
+//   again (S into one of two TMEM buffers, so a block's S and Z are computed while the math
+//   warps work on the previous block), the math warps average the G rows of a token with
+//   warp shuffles, accumulate the loss and write gz into TMEM, and d idx_q += gz idx_k
+//   accumulates in TMEM.  It leaves each 128-row group's main lse2 (per row) and lseI2 (per
+//   token) as one 1 KiB record.
 // * keys (key-block order over the tiles that selected the block, as in the dK/dV pass of
 //   the backward): S^T = K Q^T and Z^T = idx_k idx_q^T with the keys on the TMEM lanes, so a
 //   token's G rows are adjacent columns; gz^T goes to TMEM and d idx_k += gz^T idx_q
 //   accumulates there over all of the CTA's groups before one set of vector atomics.
-// Warps: 8 elementwise warps (two per TMEM lane quadrant, each taking half of the columns),
-// a TMA producer and two MMA issuers (a single thread's stream of N = 128 MMAs with commits
-// in it keeps the tensor core busy only ~60 % of the time).  Every wait is bounded.
+// Warps: 16 elementwise warps (four per TMEM lane quadrant, each taking a quarter of the
+// columns; 8 for G = 32, where a thread needs more registers than 608 threads leave), a TMA
+// producer and two MMA issuers (a single thread's stream of N = 128 MMAs with commits in it
+// keeps the tensor core busy only ~60 % of the time).  The elementwise work waits mostly on
+// the latency of its own loads and exponentials, so four warps per quadrant, not two, keep
+// the schedulers busy.  Every wait is bounded.
 #include "common.cuh"
 #include "index_kl_tc.cuh"
 #include "ptx.cuh"
@@ -42,9 +47,6 @@ constexpr int kRows = 128;
 constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;           // [2 chunks][128 rows][128 B]
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 352;                               // 8 math warps, producer, 2 MMA
-constexpr int kProducerWarp = 8, kMmaWarp = 9;             // MMA issuers: warps 9, 10
-constexpr int kMathWarps = 8;                               // two per TMEM lane quadrant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);
 constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);
@@ -76,12 +78,6 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_smem, uint32_
   }
 }
 
-// Column of bf16 chunk c (32 values packed into 16 columns) written over an fp32 region of
-// 128 columns: chunks 0-1 over the region's columns 0-31, chunks 2-3 over 96-127, so each of
-// the two warps of a lane quadrant (columns 0-63 / 64-127) overwrites only columns it has
-// itself loaded.
-__device__ __forceinline__ int p_col(int c) { return c < 2 ? c * 16 : 96 + (c - 2) * 16; }
-
 __device__ __forceinline__ void raise_abort(int* abort_flag, int* status, int code) {
   *abort_flag = 1;
   if (status) atomicExch(status, code);
@@ -96,16 +92,26 @@ struct __align__(1024) SmemR {
   uint8_t ik[2][kTileBytes];
   uint64_t q_full, ring_full[2], ring_empty[2];
   uint64_t z_full[2], z_free[2], pass1_done;
-  uint64_t s_full, g_full, dq_done, drain[2];
-  float half_ml[2][2][kRows];   // pass 1: [column half][max, sum][row]
+  uint64_t s_full[2], g_full[2], dq_done[2], z_free2, drain[2];
+  float part_ml[4][2][kRows];   // pass 1: [column part][max, sum][row]
   int blocks[kMaxSel];
   int n_sel;
   uint32_t tmem_base;
   int abort;
 };
 
+// Warps of the query-tile pass: 4 math warps per TMEM lane quadrant (each a quarter of the
+// key columns) when a thread of 608 has the registers (G <= 16), else 2.
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+struct RowsWarps {
+  static constexpr int kPerQuad = G <= 16 ? 4 : 2;
+  static constexpr int kMath = 4 * kPerQuad;
+  static constexpr int kProducer = kMath, kMma = kMath + 1;
+  static constexpr int kThreads = (kMath + 3) * 32;
+};
+
+template <int G>
+__global__ void __launch_bounds__(RowsWarps<G>::kThreads, 1)
 kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ik,
                   const __nv_bfloat16* __restrict__ idx_q, const int32_t* __restrict__ sel,
@@ -121,6 +127,7 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const int bg = blockIdx.z, b = bg / p.Hkv, g = bg % p.Hkv;
   const int t0 = m * kQt + part * kTokPerGroup;
   const volatile int* abort = &s.abort;
+  using W = RowsWarps<G>;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&s.q_full, 1);
@@ -128,12 +135,15 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_init(&s.ring_full[i], 1);
       ptx::mbar_init(&s.ring_empty[i], 1);
       ptx::mbar_init(&s.z_full[i], 1);
-      ptx::mbar_init(&s.z_free[i], kMathWarps);
+      ptx::mbar_init(&s.z_free[i], W::kMath);
     }
-    ptx::mbar_init(&s.pass1_done, kMathWarps);
-    ptx::mbar_init(&s.s_full, 1);
-    ptx::mbar_init(&s.g_full, kMathWarps);
-    ptx::mbar_init(&s.dq_done, 1);
+    ptx::mbar_init(&s.pass1_done, W::kMath);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.s_full[i], 1);
+      ptx::mbar_init(&s.g_full[i], W::kMath);
+      ptx::mbar_init(&s.dq_done[i], 1);
+    }
+    ptx::mbar_init(&s.z_free2, W::kMath);
     ptx::mbar_init(&s.drain[0], 1);
     ptx::mbar_init(&s.drain[1], 1);
     s.abort = 0;
@@ -176,11 +186,12 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   ptx::tc_fence_after_sync();
   const uint32_t tmem = s.tmem_base;
   const int n_sel = s.n_sel;
-  // TMEM: pass 1 Z in [0,128) / [128,256) alternately; pass 2 S [0,128) (gz bf16 over its
-  // first 64), Z [128,256), dIQ [256,384)
-  constexpr uint32_t kColS = 0, kColZ = 128, kColDQ = 256;
+  // TMEM: pass 1 Z in [0,128) / [128,256) alternately; pass 2 S in [0,128) / [384,512)
+  // alternately by block (gz bf16 over part of it), Z [128,256), dIQ [256,384)
+  constexpr uint32_t kColZ = 128, kColDQ = 256;
+  auto col_s = [](int j) -> uint32_t { return (j & 1) ? 384u : 0u; };
 
-  if (warp == kProducerWarp) {
+  if (warp == W::kProducer) {
     int issued = 0;
     bool ok = true;
     // test hook: issue nothing, so the consumers' bounded waits run out
@@ -215,12 +226,12 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int rr = issued > 2 ? issued - 2 : 0; rr < issued; ++rr)
         ptx::mbar_wait_timed(&s.ring_full[rr & 1], (rr >> 1) & 1);
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+  } else if (warp == W::kMma || warp == W::kMma + 1) {
     // warp 9: pass 1's Z and pass 2's S and Z; warp 10: pass 2's dIQ += gz idx_k (a single
     // thread's stream of N = 128 MMAs with commits keeps the tensor core busy only ~60 %
     // of the time).  S and Z of block j overwrite the gz of block j-1, so they wait for
     // warp 10's product of block j-1.
-    const int who = warp - kMmaWarp;
+    const int who = warp - W::kMma;
     bool ok = true, issued_any = false;
     const uint32_t qa = ptx::smem_u32(s.q), za = ptx::smem_u32(s.iqr);
     if (who == 0) {
@@ -241,32 +252,35 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ok = ptx::mbar_wait(&s.pass1_done, 0, abort) && ptx::mbar_wait(&s.q_full, 0, abort);
       for (int j = 0; ok && j < n_sel; ++j) {                // pass 2: S and Z
         const int rr = n_sel + j, st = rr & 1;
+        // S of block j goes where block j-2's gz was (its dIQ product has read it); Z
+        // where block j-1's Z was (the math warps have loaded it)
         if (!ptx::mbar_wait(&s.ring_full[st], (rr >> 1) & 1, abort) ||
-            (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort))) { ok = false; break; }
+            (j > 1 && !ptx::mbar_wait(&s.dq_done[j & 1], ((j >> 1) & 1) ^ 1, abort)) ||
+            (j > 0 && !ptx::mbar_wait(&s.z_free2, (j - 1) & 1, abort))) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
-          mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[st]), kBk * kRowBytes, kIdescKK);
+          mma_kk(tmem + col_s(j), qa, ptx::smem_u32(s.k[st]), kBk * kRowBytes, kIdescKK);
           mma_kk(tmem + kColZ, za, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
-          ptx::umma_commit(&s.s_full);
+          ptx::umma_commit(&s.s_full[j & 1]);
         }
         __syncwarp();
       }
     } else {
       for (int j = 0; ok && j < n_sel; ++j) {                // pass 2: dIQ += gz idx_k
         const int rr = n_sel + j, st = rr & 1;
-        if (!ptx::mbar_wait(&s.g_full, j & 1, abort)) { ok = false; break; }
+        if (!ptx::mbar_wait(&s.g_full[j & 1], (j >> 1) & 1, abort)) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
-          // gz (rows x keys) from TMEM (keys 64-127 at columns 96-127), idx_k as the
-          // MN-major B operand; block j's ring stage is free once this product finishes
-          // (its S and Z completed before the math warps formed gz)
+          // gz (rows x keys) from TMEM (keys 32c .. 32c+31 packed at columns 32c .. 32c+15),
+          // idx_k as the MN-major B operand; block j's ring stage is free once this product
+          // finishes (its S and Z completed before the math warps formed gz)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            ptx::umma_bf16_ts(tmem + kColDQ, tmem + kColS + kk * 8 + (kk >= 4 ? 64 : 0),
+            ptx::umma_bf16_ts(tmem + kColDQ, tmem + col_s(j) + 32 * (kk >> 1) + (kk & 1) * 8,
                               ptx::smem_desc_mn_sw128(ptx::smem_u32(s.ik[st]) + kk * 16 * kRowBytes,
                                                       kBk * kRowBytes, 1024),
                               kIdescMN, (j > 0 || kk > 0) ? 1u : 0u);
-          ptx::umma_commit(&s.dq_done);
+          ptx::umma_commit(&s.dq_done[j & 1]);
           ptx::umma_commit(&s.ring_empty[st]);
         }
         issued_any = true;
@@ -279,8 +293,10 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
-    // ------------------------- math warps 0-7: warp w takes row quadrant w % 4 and the key
-    // columns (and d idx_q columns) 64 (w / 4) .. +63
+    // ------------------------- math warps: warp w takes row quadrant w % 4 and the key
+    // columns (and d idx_q columns) of its part w / 4 (kCols32 chunks of 32)
+    constexpr int kParts = W::kPerQuad;
+    constexpr int kCols32 = 4 / kParts;
     const int quad = warp & 3, half = warp >> 2;
     const int r = quad * 32 + lane;
     const int t = t0 + r / G, hh = r % G, h = g * G + hh;
@@ -297,17 +313,17 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const int buf = j & 1, lim = t - s.blocks[j] * kBk;
       if (!ptx::mbar_wait(&s.z_full[buf], (j >> 1) & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      uint32_t zv[2][32];
+      uint32_t zv[kCols32][32];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-        ptx::tmem_ld_x32(tmem + lane_off + buf * 128 + (2 * half + u) * 32, zv[u]);
+      for (int u = 0; u < kCols32; ++u)
+        ptx::tmem_ld_x32(tmem + lane_off + buf * 128 + (kCols32 * half + u) * 32, zv[u]);
       ptx::tmem_ld_wait();
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s.z_free[buf]);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = 2 * half + u;
+      for (int u = 0; u < kCols32; ++u) {
+        const int c = kCols32 * half + u;
         float zk[32 / G];                                    // this lane's keys of the chunk
         float cm = -INFINITY;
 #pragma unroll
@@ -341,11 +357,15 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     // every math warp reaches this barrier exactly once (also after a failed wait)
-    s.half_ml[half][0][r] = mI;
-    s.half_ml[half][1][r] = lI;
-    asm volatile("bar.sync 1, %0;" ::"r"(kMathWarps * 32) : "memory");
-    {
-      const float mo = s.half_ml[half ^ 1][0][r], lo = s.half_ml[half ^ 1][1][r];
+    s.part_ml[half][0][r] = mI;
+    s.part_ml[half][1][r] = lI;
+    asm volatile("bar.sync 1, %0;" ::"r"(W::kMath * 32) : "memory");
+    // the parts, combined in part order (every part's warp gets the same result)
+    mI = -INFINITY;
+    lI = 0.f;
+#pragma unroll
+    for (int q = 0; q < kParts; ++q) {
+      const float mo = s.part_ml[q][0][r], lo = s.part_ml[q][1][r];
       const float mn = fmaxf(mI, mo);
       if (mn != -INFINITY) {
         lI = lI * ex2(mI - mn) + lo * ex2(mo - mn);
@@ -371,18 +391,23 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float lsum = 0.f;
     for (int j = 0; ok && j < n_sel; ++j) {
       const int lim = t - s.blocks[j] * kBk;
-      if (!ptx::mbar_wait(&s.s_full, j & 1, abort)) { ok = false; break; }
+      if (!ptx::mbar_wait(&s.s_full[j & 1], (j >> 1) & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      uint32_t sv[2][32], zv[2][32];
+      const uint32_t cs = col_s(j);
+      uint32_t sv[kCols32][32], zv[kCols32][32];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
-        ptx::tmem_ld_x32(tmem + lane_off + kColZ + (2 * half + u) * 32, zv[u]);
+      for (int u = 0; u < kCols32; ++u) {
+        ptx::tmem_ld_x32(tmem + lane_off + cs + (kCols32 * half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + kColZ + (kCols32 * half + u) * 32, zv[u]);
       }
       ptx::tmem_ld_wait();
+      // Z is in registers: the next block's Z may overwrite it
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.z_free2);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = 2 * half + u;
+      for (int u = 0; u < kCols32; ++u) {
+        const int c = kCols32 * half + u;
         uint32_t pk[16];
 #pragma unroll
         for (int e0 = 0; e0 < 32; e0 += G) {
@@ -417,21 +442,22 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           for (int x = 0; x < G; x += 2)
             pk[(e0 + x) >> 1] = pack_bf16x2(hh == x ? gz : 0.f, hh == x + 1 ? gz : 0.f);
         }
-        // gz over S columns this warp loaded (p_col)
-        ptx::tmem_st_x16(tmem + lane_off + kColS + p_col(c), pk);
+        // gz over S columns this warp loaded: chunk c at columns 32c .. 32c+15
+        ptx::tmem_st_x16(tmem + lane_off + cs + 32 * c, pk);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s.g_full);
+      if (lane == 0) ptx::mbar_arrive(&s.g_full[j & 1]);
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x703);
-    const bool have = ok && n_sel > 0 && ptx::mbar_wait(&s.dq_done, (n_sel - 1) & 1, abort);
+    const bool have = ok && n_sel > 0 &&
+                      ptx::mbar_wait(&s.dq_done[(n_sel - 1) & 1], ((n_sel - 1) >> 1) & 1, abort);
     if (have) ptx::tc_fence_after_sync();
     float* dst = d_idx_q + (((size_t)b * p.Sq + (valid ? t : 0)) * p.Hkv + g) * kD;
 #pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int c = 2 * half + u;
+    for (int u = 0; u < kCols32; ++u) {
+      const int c = kCols32 * half + u;
       uint32_t v[32];
       if (have) {
         ptx::tmem_ld_x32(tmem + lane_off + kColDQ + c * 32, v);
@@ -487,8 +513,18 @@ struct __align__(1024) SmemK {
   int abort;
 };
 
+// Warps of the key-block pass: 4 math warps per TMEM lane quadrant (each a quarter of a
+// group's rows) when a quarter holds whole packed gz^T columns (G <= 16), else 2.
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+struct KeysWarps {
+  static constexpr int kPerQuad = G <= 16 ? 4 : 2;
+  static constexpr int kMath = 4 * kPerQuad;
+  static constexpr int kProducer = kMath, kMma = kMath + 1;
+  static constexpr int kThreads = (kMath + 3) * 32;
+};
+
+template <int G>
+__global__ void __launch_bounds__(KeysWarps<G>::kThreads, 1)
 kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ik, const __grid_constant__ CUtensorMap tm_iq,
                   const uint32_t* __restrict__ bits, const float* __restrict__ rowstat,
@@ -531,7 +567,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const volatile int* abort = &s.abort;
 
   // the idx_q rows past a group's tokens stay zero (the copies write only kTok rows)
-  for (int i = threadIdx.x; i < 2 * kIqBytes / 16; i += kThreads)
+  using W = KeysWarps<G>;
+  for (int i = threadIdx.x; i < 2 * kIqBytes / 16; i += W::kThreads)
     reinterpret_cast<uint4*>(&s.iq[0][0])[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     ptx::mbar_init(&s.kv_full, 1);
@@ -541,7 +578,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(&s.s_full[i], 1);
-      ptx::mbar_init(&s.p_full[i], kMathWarps);
+      ptx::mbar_init(&s.p_full[i], W::kMath);
       ptx::mbar_init(&s.acc_done[i], 1);
       ptx::mbar_init(&s.drain[i], 1);
     }
@@ -569,7 +606,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   auto col_g = [](int b) -> uint32_t { return b == 0 ? 192u : 224u; };
   constexpr uint32_t kIdescZ = ptx::idesc_bf16_f32(128, kNTok, 0, 0);
 
-  if (warp == kProducerWarp) {
+  if (warp == W::kProducer) {
     int issued = 0;
     bool ok = true;
     if (lane == 0) {
@@ -604,10 +641,10 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int gi = issued > 2 ? issued - 2 : 0; gi < issued; ++gi)
         ptx::mbar_wait_timed(&s.g_full[gi & 1], (gi >> 1) & 1);
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+  } else if (warp == W::kMma || warp == W::kMma + 1) {
     // warp 9: S^T and Z^T of each group (after the math warps released the previous
     // group's); warp 10: dIK += gz^T idx_q
-    const int who = warp - kMmaWarp;
+    const int who = warp - W::kMma;
     bool ok = ptx::mbar_wait(&s.kv_full, 0, abort);
     bool issued_any = false;
     const uint32_t ka = ptx::smem_u32(s.k), ia = ptx::smem_u32(s.ik);
@@ -648,15 +685,18 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
-    // ----------------- math warps 0-7: one key of the block per lane (quadrant w % 4); warp
-    // w takes the group rows 64 (w / 4) .. +63, i.e. tokens kTok / 2 (w / 4) .. +kTok / 2, and
-    // the d idx_k columns 64 (w / 4) .. +63
-    constexpr int kHalfTok = kTok / 2;
-    const int quad = warp & 3, half = warp >> 2;
+    // ----------------- math warps: one key of the block per lane (quadrant w % 4); warp w
+    // takes the group rows kRowsW (w / 4) .. +kRowsW - 1, i.e. its tokens, and the d idx_k
+    // columns kRowsW (w / 4) .. +kRowsW - 1
+    constexpr int kParts = W::kPerQuad;
+    constexpr int kRowsW = kRows / kParts;                    // rows of a warp
+    constexpr int kTokW = kTok / kParts;                      // tokens of a warp
+    constexpr int kCols32 = kRowsW / 32;                      // 32-column chunks of a warp
+    const int quad = warp & 3, part_w = warp >> 2;
     const int key = blk * kBk + quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const float c1 = p.sm_scale * kLog2e, c2 = p.index_scale * kLog2e;
-    if (half == 0 && kTok < 16) {
+    if (part_w == 0 && kTok < 16) {
       // gz^T columns past the group's tokens (the padding up to the UMMA's K of 16) stay zero
       uint32_t z8[8];
 #pragma unroll
@@ -675,39 +715,37 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // the d idx_k MMA of the group that last used this gz^T buffer has read it
           (gi >= kNBuf && !ptx::mbar_wait(&s.acc_done[bf], ph ^ 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      uint32_t sv[2][32];
+      uint32_t sv[kCols32][32];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-        ptx::tmem_ld_x32(tmem + lane_off + col_s(bf) + (2 * half + u) * 32, sv[u]);
+      for (int u = 0; u < kCols32; ++u)
+        ptx::tmem_ld_x32(tmem + lane_off + col_s(bf) + (kCols32 * part_w + u) * 32, sv[u]);
       // this warp's tokens' Z^T columns (loaded 16 at a time; a 16-column load that runs past
       // the Z^T columns reads unused TMEM and those values are not used)
-      constexpr int kZLoads = kHalfTok < 16 ? 1 : kHalfTok / 16;
+      constexpr int kZLoads = kTokW < 16 ? 1 : kTokW / 16;
       uint32_t zv[kZLoads][16];
 #pragma unroll
       for (int c = 0; c < kZLoads; ++c)
-        ptx::tmem_ld_x16(tmem + lane_off + col_z(bf) + half * kHalfTok + c * 16, zv[c]);
+        ptx::tmem_ld_x16(tmem + lane_off + col_z(bf) + part_w * kTokW + c * 16, zv[c]);
       ptx::tmem_ld_wait();
-      float pt[kHalfTok];
+      float pt[kTokW];
 #pragma unroll
-      for (int x = 0; x < kHalfTok; ++x) pt[x] = 0.f;
+      for (int x = 0; x < kTokW; ++x) pt[x] = 0.f;
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < kCols32; ++u)
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int x = half * 64 + u * 32 + e;              // row of the group
+          const int x = part_w * kRowsW + u * 32 + e;        // row of the group
           const int tok = (u * 32 + e) / G;                  // this warp's token index
-          if (key <= t0 + half * kHalfTok + tok)
+          if (key <= t0 + part_w * kTokW + tok)
             pt[tok] += ex2(fmaf(__uint_as_float(sv[u][e]), c1, -s.rec[st][x]));
         }
-      uint32_t pk[16];
+      uint32_t pk[kTokW / 2 > 0 ? kTokW / 2 : 1];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) pk[x] = 0u;
-#pragma unroll
-      for (int tk = 0; tk < kHalfTok; tk += 2) {
+      for (int tk = 0; tk < kTokW; tk += 2) {
         float gz2[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const int tok = half * kHalfTok + tk + u;          // token of the group
+          const int tok = part_w * kTokW + tk + u;            // token of the group
           const bool vis = key <= t0 + tok && t0 + tok < p.Sq;
           const float pi = vis ? ex2(fmaf(__uint_as_float(zv[(tk + u) / 16][(tk + u) % 16]), c2,
                                           -s.rec[st][kRows + tok]))
@@ -717,11 +755,11 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         pk[tk >> 1] = pack_bf16x2(gz2[0], gz2[1]);
       }
       // this warp's tokens' gz^T columns (2 tokens per column)
-      const uint32_t gcol = tmem + lane_off + col_g(bf) + half * (kHalfTok / 2);
-      if constexpr (kHalfTok / 2 == 1) ptx::tmem_st_x1(gcol, pk);
-      else if constexpr (kHalfTok / 2 == 2) ptx::tmem_st_x2(gcol, pk);
-      else if constexpr (kHalfTok / 2 == 4) ptx::tmem_st_x4(gcol, pk);
-      else if constexpr (kHalfTok / 2 == 8) ptx::tmem_st_x8(gcol, pk);
+      const uint32_t gcol = tmem + lane_off + col_g(bf) + part_w * (kTokW / 2);
+      if constexpr (kTokW / 2 == 1) ptx::tmem_st_x1(gcol, pk);
+      else if constexpr (kTokW / 2 == 2) ptx::tmem_st_x2(gcol, pk);
+      else if constexpr (kTokW / 2 == 4) ptx::tmem_st_x4(gcol, pk);
+      else if constexpr (kTokW / 2 == 8) ptx::tmem_st_x8(gcol, pk);
       else ptx::tmem_st_x16(gcol, pk);
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
@@ -737,8 +775,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool in_range = key < p.Sk;
       float4* dst = reinterpret_cast<float4*>(d_idx_k + ((size_t)b * p.Sk + (in_range ? key : 0)) * kD);
 #pragma unroll 1
-      for (int u = 0; u < 2; ++u) {
-        const int c = 2 * half + u;
+      for (int u = 0; u < kCols32; ++u) {
+        const int c = kCols32 * part_w + u;
         uint32_t a[32];
         ptx::tmem_ld_x32(tmem + lane_off + kColDK + c * 32, a);
         ptx::tmem_ld_wait();
@@ -782,7 +820,7 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.Qt * G / kRows, p.nR, p.B * p.Hkv);
-    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, (const __nv_bfloat16*)idx_q, sel, lse,
+    kern<<<grid, RowsWarps<G>::kThreads, smem, st>>>(tq, tk, tik, (const __nv_bfloat16*)idx_q, sel, lse,
                                        rowstat, loss, d_idx_q, p, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -794,7 +832,7 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
     const int words = (p.nR + 31) / 32;
     const int wpc = tiles_per_cta(p) / 32;
     dim3 grid((words + wpc - 1) / wpc, p.nB, p.B * p.Hkv);
-    kern<<<grid, kThreads, smem, st>>>(tq, tk, tik, tiq, bits, rowstat, d_idx_k, p, words, wpc,
+    kern<<<grid, KeysWarps<G>::kThreads, smem, st>>>(tq, tk, tik, tiq, bits, rowstat, d_idx_k, p, words, wpc,
                                        status);
     e = cudaGetLastError();
   }
