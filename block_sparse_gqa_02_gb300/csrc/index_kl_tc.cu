@@ -227,10 +227,11 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::mbar_wait_timed(&s.ring_full[rr & 1], (rr >> 1) & 1);
     }
   } else if (warp == W::kMma || warp == W::kMma + 1) {
-    // warp 9: pass 1's Z and pass 2's S and Z; warp 10: pass 2's dIQ += gz idx_k (a single
-    // thread's stream of N = 128 MMAs with commits keeps the tensor core busy only ~60 %
-    // of the time).  S and Z of block j overwrite the gz of block j-1, so they wait for
-    // warp 10's product of block j-1.
+    // the first issuer: pass 1's Z and pass 2's S and Z; the second: pass 2's dIQ += gz
+    // idx_k (a single thread's stream of N = 128 MMAs with commits keeps the tensor core
+    // busy only ~60 % of the time).  S of block j goes over the gz of block j-2, so it waits
+    // for the second issuer's product of block j-2; Z over block j-1's Z, once the math
+    // warps have loaded it.
     const int who = warp - W::kMma;
     bool ok = true, issued_any = false;
     const uint32_t qa = ptx::smem_u32(s.q), za = ptx::smem_u32(s.iqr);
@@ -642,8 +643,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::mbar_wait_timed(&s.g_full[gi & 1], (gi >> 1) & 1);
     }
   } else if (warp == W::kMma || warp == W::kMma + 1) {
-    // warp 9: S^T and Z^T of each group (after the math warps released the previous
-    // group's); warp 10: dIK += gz^T idx_q
+    // the first issuer: S^T and Z^T of each group (after the math warps released the
+    // buffer's previous group); the second: dIK += gz^T idx_q
     const int who = warp - W::kMma;
     bool ok = ptx::mbar_wait(&s.kv_full, 0, abort);
     bool issued_any = false;

@@ -21,10 +21,11 @@
 //   the elementwise warps form P^T and dS^T there, and dV += P^T dO, dK += dS^T Q accumulate
 //   in TMEM over all of the CTA's groups.  A CTA adds its dK / dV to the fp32 outputs with
 //   vector atomics (a heavily selected block is split over several CTAs).
-// Warps: 8 elementwise warps (two per TMEM lane quadrant, each taking half of the columns of
-// S / dP or S^T / dP^T), a TMA producer and two MMA issuers (a single thread's stream of
-// N = 128 MMAs with commits in it keeps the tensor core busy only ~60 % of the time).  Every
-// wait is bounded.
+// Warps: 16 elementwise warps (four per TMEM lane quadrant, each taking a quarter of the
+// columns of S / dP or S^T / dP^T: with two, the warps waited mostly on the latency of their
+// own loads and exponentials), a TMA producer and two MMA issuers (a single thread's stream
+// of N = 128 MMAs with commits in it keeps the tensor core busy only ~60 % of the time).
+// Every wait is bounded.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sparse_backward_tc.cuh"
@@ -41,9 +42,9 @@ constexpr int kRows = 128;                              // rows of one Q group
 constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;       // [2 chunks][128 rows][128 B] = 32 KiB
 constexpr int kMaxSel = 256;
-constexpr int kThreads = 352;                           // 8 math warps, producer, 2 MMA issuers
-constexpr int kProducerWarp = 8, kMmaWarp = 9;       // MMA issuers: warps 9 and 10
-constexpr int kMathWarps = 8;                           // two per TMEM lane quadrant
+constexpr int kMathWarps = 16;                          // four per TMEM lane quadrant
+constexpr int kProducerWarp = kMathWarps, kMmaWarp = kMathWarps + 1;   // MMA issuers: 17, 18
+constexpr int kThreads = (kMathWarps + 3) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);   // both operands K-major
 constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);   // B MN-major
@@ -73,22 +74,18 @@ __device__ __forceinline__ void mma_kk(uint32_t d_tmem, uint32_t a_smem, uint32_
 }
 
 // D[tmem] (+)= A[tmem, 128 x 128 bf16] B[smem, MN-major 128 x 128], the reduction over the
-// 128 rows of B: dQ += dS K, dV += P^T dO, dK += dS^T Q.  A's second half (K 64..127) sits at
-// columns 96..127 of its region when split (see p_col), else right after the first.
+// 128 rows of B: dQ += dS K, dV += P^T dO, dK += dS^T Q.  When split, A's 32-row chunk c
+// (16 packed columns) sits at columns 32c .. 32c+15 of its region (the columns the chunk's
+// fp32 values came from); else the chunks follow one another.
 __device__ __forceinline__ void mma_tmn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
                                         bool accumulate, bool split = false) {
 #pragma unroll
   for (int kk = 0; kk < 128 / 16; ++kk)
-    ptx::umma_bf16_ts(d_tmem, a_tmem + kk * 8 + (split && kk >= 4 ? 64 : 0),
+    ptx::umma_bf16_ts(d_tmem, a_tmem + (split ? 32 * (kk >> 1) + (kk & 1) * 8 : kk * 8),
                       ptx::smem_desc_mn_sw128(b_smem + kk * 16 * kRowBytes, kRows * kRowBytes, 1024),
                       kIdescMN, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Column of bf16 chunk c (32 values packed into 16 columns) written over an fp32 region of
-// 128 columns: chunks 0-1 over the region's columns 0-31, chunks 2-3 over 96-127, so each of
-// the two warps of a lane quadrant (columns 0-63 / 64-127) overwrites only columns it has
-// itself loaded.
-__device__ __forceinline__ int p_col(int c) { return c < 2 ? c * 16 : 96 + (c - 2) * 16; }
 
 __device__ __forceinline__ void raise_abort(int* abort_flag, int* status, int code) {
   *abort_flag = 1;
@@ -121,6 +118,7 @@ struct __align__(1024) SmemQ {
   uint64_t qd_full;
   uint64_t kv_full[2], kv_empty[2];
   uint64_t s_full, s_free, ds_full, dq_done, drain[2];
+  float dsum[kRows];
   int blocks[kMaxSel];
   int n_sel;
   uint32_t tmem_base;
@@ -227,8 +225,9 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------- MMA issuers
-    // warp 9: S = Q K^T and dP = dO V^T of each block (into TMEM once the math warps have
-    // read the previous block's); warp 10: dQ += dS K once the math warps have written dS.
+    // the first issuer: S = Q K^T and dP = dO V^T of each block (into TMEM once the math
+    // warps have read the previous block's); the second: dQ += dS K once the math warps
+    // have written dS.
     // One thread's stream of N = 128 MMAs with commits keeps the tensor core busy only
     // ~60 % of the time; two streams fill it.
     const int who = warp - kMmaWarp;
@@ -270,8 +269,8 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
-    // ------------------------- math warps 0-7: warp w takes row quadrant w % 4 and the key
-    // columns (and dQ columns) 64 (w / 4) .. +63
+    // ------------------------- math warps 0-15: warp w takes row quadrant w % 4 and the key
+    // columns (and dQ columns) 32 (w / 4) .. +31
     const int quad = warp & 3, half = warp >> 2;
     const int r = quad * 32 + lane;
     const int R = part * kRows + r;                      // row within the tile's Qt*G rows
@@ -280,9 +279,10 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     const bool valid = t < p.Sq;
     const float c1 = p.sm_scale * kLog2e;
     const size_t row_off = (((size_t)b * p.Sq + (valid ? t : 0)) * p.Hq + h) * kD;
-    // D = dout . out of this row (both warps of the quadrant need it)
+    // D = dout . out of this row, formed by the quadrant's first warp and shared (every warp
+    // of the quadrant needs it)
     float dsum = 0.f;
-    if (valid) {
+    if (valid && half == 0) {
       const uint4* o4 = reinterpret_cast<const uint4*>(out + row_off);
       const uint4* d4 = reinterpret_cast<const uint4*>(dout + row_off);
 #pragma unroll 4
@@ -297,6 +297,9 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
     }
+    if (half == 0) s.dsum[r] = dsum;
+    asm volatile("bar.sync 1, %0;" ::"r"(kMathWarps * 32) : "memory");
+    dsum = s.dsum[r];
     const float lse2 = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
     if (half == 0) {
       // the group's record for the dK/dV pass: lse2 of its 128 rows, then their D
@@ -313,11 +316,11 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       const int lim = t - blk * kBk;                       // visible columns: c <= lim
-      uint32_t sv[2][32], dv[2][32];
+      uint32_t sv[1][32], dv[1][32];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
-        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (2 * half + u) * 32, dv[u]);
+      for (int u = 0; u < 1; ++u) {
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + (half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (half + u) * 32, dv[u]);
       }
       ptx::tmem_ld_wait();
       // this warp's S / dP columns are in registers: the next block may overwrite them
@@ -325,8 +328,8 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s.s_free);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = 2 * half + u;
+      for (int u = 0; u < 1; ++u) {
+        const int c = half + u;
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -351,13 +354,13 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     bool have = ok && n_sel > 0 && ptx::mbar_wait(&s.dq_done, (n_sel - 1) & 1, abort);
     if (ok && n_sel > 0 && !have && lane == 0) raise_abort(&s.abort, status, 0x504);
     if (have) ptx::tc_fence_after_sync();
-    // dq = sm_scale * dQ (zero for a row with no visible key), this warp's 64 columns;
+    // dq = sm_scale * dQ (zero for a row with no visible key), this warp's 32 columns;
     // tcgen05.ld is warp-collective, so every lane loads (`have` is the same in the whole
     // warp) and valid rows store
     float4* dst = reinterpret_cast<float4*>(dq + row_off);
 #pragma unroll 1
-    for (int u = 0; u < 2; ++u) {
-      const int c = 2 * half + u;
+    for (int u = 0; u < 1; ++u) {
+      const int c = half + u;
       uint32_t v[32];
       if (have) {
         ptx::tmem_ld_x32(tmem + lane_off + kColDQ + c * 32, v);
@@ -512,7 +515,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     // ------------------------------------------------------------- MMA issuers
-    // warp 9: S^T = K Q^T, then dK += dS^T Q; warp 10: dP^T = V dO^T, then dV += P^T dO.
+    // the first issuer: S^T = K Q^T, then dK += dS^T Q; the second: dP^T = V dO^T, then
+    // dV += P^T dO.
     // P^T is written over S^T and read by dV, dS^T over dP^T and read by dK, so each
     // issuer's next product waits for the other issuer's last one, never for its own.
     const int who = warp - kMmaWarp;
@@ -549,8 +553,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_wait_timed(&s.drain[who], 0);
     }
   } else {
-    // ----------------- math warps 0-7: one key of the block per lane (quadrant w % 4); warp
-    // w takes the group rows (and dV / dK columns) 64 (w / 4) .. +63
+    // ----------------- math warps 0-15: one key of the block per lane (quadrant w % 4); warp
+    // w takes the group rows (and dV / dK columns) 32 (w / 4) .. +31
     const int quad = warp & 3, half = warp >> 2;
     const int key = blk * kBk + quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -567,16 +571,16 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
           !ptx::mbar_wait(&s.s_full, gi & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      uint32_t sv[2][32], dpv[2][32];
+      uint32_t sv[1][32], dpv[1][32];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + (2 * half + u) * 32, sv[u]);
-        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (2 * half + u) * 32, dpv[u]);
+      for (int u = 0; u < 1; ++u) {
+        ptx::tmem_ld_x32(tmem + lane_off + kColS + (half + u) * 32, sv[u]);
+        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (half + u) * 32, dpv[u]);
       }
       ptx::tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = 2 * half + u;
+      for (int u = 0; u < 1; ++u) {
+        const int c = half + u;
         uint32_t pp[16], dd[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -590,9 +594,9 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
           pp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
           dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
         }
-        // P^T / dS^T over columns this warp loaded (p_col)
-        ptx::tmem_st_x16(tmem + lane_off + kColS + p_col(c), pp);
-        ptx::tmem_st_x16(tmem + lane_off + kColDP + p_col(c), dd);
+        // P^T / dS^T over columns this warp loaded: chunk c at columns 32c .. 32c+15
+        ptx::tmem_st_x16(tmem + lane_off + kColS + 32 * c, pp);
+        ptx::tmem_st_x16(tmem + lane_off + kColDP + 32 * c, dd);
       }
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
@@ -609,8 +613,8 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       float4* dvr = reinterpret_cast<float4*>(dv + ((size_t)bg * p.Sk + (in_range ? key : 0)) * kD);
       float4* dkr = reinterpret_cast<float4*>(dk + ((size_t)bg * p.Sk + (in_range ? key : 0)) * kD);
 #pragma unroll 1
-      for (int u = 0; u < 2; ++u) {
-        const int c = 2 * half + u;
+      for (int u = 0; u < 1; ++u) {
+        const int c = half + u;
         uint32_t a[32], bk[32];
         ptx::tmem_ld_x32(tmem + lane_off + kColDV + c * 32, a);
         ptx::tmem_ld_x32(tmem + lane_off + kColDK + c * 32, bk);
