@@ -12,18 +12,23 @@
 //   d idx_q[t,g] = index_scale sum_j gz_j idx_k[j];  d idx_k[j] += index_scale gz_j idx_q[t,g].
 //
 // Two kernels:
-// * rows (query-tile order, one CTA per 128 (token, head) rows like the forward): a first
-//   pass over the blocks forms lseI2 from Z = idx_q idx_k^T, with each row's idx_q replicated
-//   so that every row of a token holds its token's index logits; a second pass forms S and Z
-//   again (S into one of two TMEM buffers, so a block's S and Z are computed while the math
-//   warps work on the previous block), the math warps average the G rows of a token with
-//   warp shuffles, accumulate the loss and write gz into TMEM, and d idx_q += gz idx_k
-//   accumulates in TMEM.  It leaves each 128-row group's main lse2 (per row) and lseI2 (per
-//   token) as one 1 KiB record.
+// * rows (query-tile order, one CTA per 128 (token, head) rows like the forward): a pass
+//   over the blocks forms lseI2 from Z = idx_q idx_k^T, with each row's idx_q replicated so
+//   that every row of a token holds its token's index logits, and leaves each 128-row
+//   group's main lse2 (per row) and lseI2 (per token) as one 1 KiB record.  With G < 8 a
+//   second pass forms S and Z again (S into one of two TMEM buffers, so a block's S and Z
+//   are computed while the math warps work on the previous block), the math warps average
+//   the G rows of a token with warp shuffles, accumulate the loss and write gz into TMEM,
+//   and d idx_q += gz idx_k accumulates in TMEM.  With G >= 8 it only zeroes d idx_q.
 // * keys (key-block order over the tiles that selected the block, as in the dK/dV pass of
 //   the backward): S^T = K Q^T and Z^T = idx_k idx_q^T with the keys on the TMEM lanes, so a
 //   token's G rows are adjacent columns; gz^T goes to TMEM and d idx_k += gz^T idx_q
-//   accumulates there over all of the CTA's groups before one set of vector atomics.
+//   accumulates there over all of the CTA's groups before one set of vector atomics.  With
+//   G >= 8 (at most 16 tokens a group) it also forms the loss terms and, per group,
+//   d idx_q^T = idx_k^T gz^T (the block's idx_k tile read MN-major, gz written K-major to
+//   shared memory) into 16 TMEM columns, which the math warps add into d idx_q with fp32
+//   atomics two groups later: the second walk of the query-tile pass, which repeated the
+//   block products the key-block pass forms anyway, is gone (32K: 4.23 -> 2.87 ms).
 // Warps: 16 elementwise warps (four per TMEM lane quadrant, each taking a quarter of the
 // columns; 8 for G = 32, where a thread needs more registers than 608 threads leave), a TMA
 // producer and two MMA issuers (a single thread's stream of N = 128 MMAs with commits in it
@@ -53,6 +58,12 @@ constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kMaxTilesPerCta = 2048;
+
+// With G >= 8 a 128-row group holds at most 16 tokens, and the key-block pass also forms
+// d idx_q (as d idx_q^T = idx_k^T gz^T per group, into 16 spare TMEM columns) and the loss,
+// so the query-tile pass only makes the walk for the index normaliser.
+template <int G>
+constexpr bool kKeysDQ = G >= 8;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -196,13 +207,14 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     bool ok = true;
     // test hook: issue nothing, so the consumers' bounded waits run out
     const int n_load = p.inject == 1 ? 0 : n_sel;
-    if (lane == 0 && n_load > 0) {
+    constexpr int kWalks = kKeysDQ<G> ? 1 : 2;
+    if (lane == 0 && n_load > 0 && !kKeysDQ<G>) {
       ptx::mbar_arrive_expect_tx(&s.q_full, kTileBytes);
       for (int kc = 0; kc < 2; ++kc)
         ptx::tma_load_4d(s.q + kc * kRows * kRowBytes, &tm_q, &s.q_full, kc * 64, g * G, t0, b);
     }
     // the block ring: pass 1 loads idx_k blocks, pass 2 idx_k and K blocks
-    for (int rr = 0; rr < 2 * n_load; ++rr) {
+    for (int rr = 0; rr < kWalks * n_load; ++rr) {
       const int st = rr & 1;
       if (!ptx::mbar_wait(&s.ring_empty[st], ((rr >> 1) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
@@ -222,7 +234,7 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x701);
     if (*abort && lane == 0 && n_load > 0) {
-      ptx::mbar_wait_timed(&s.q_full, 0);
+      if (!kKeysDQ<G>) ptx::mbar_wait_timed(&s.q_full, 0);
       for (int rr = issued > 2 ? issued - 2 : 0; rr < issued; ++rr)
         ptx::mbar_wait_timed(&s.ring_full[rr & 1], (rr >> 1) & 1);
     }
@@ -249,9 +261,9 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         issued_any = true;
         __syncwarp();
       }
-      if (ok && n_sel > 0)
+      if (ok && n_sel > 0 && !kKeysDQ<G>)
         ok = ptx::mbar_wait(&s.pass1_done, 0, abort) && ptx::mbar_wait(&s.q_full, 0, abort);
-      for (int j = 0; ok && j < n_sel; ++j) {                // pass 2: S and Z
+      for (int j = 0; ok && !kKeysDQ<G> && j < n_sel; ++j) { // pass 2: S and Z
         const int rr = n_sel + j, st = rr & 1;
         // S of block j goes where block j-2's gz was (its dIQ product has read it); Z
         // where block j-1's Z was (the math warps have loaded it)
@@ -267,7 +279,7 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncwarp();
       }
     } else {
-      for (int j = 0; ok && j < n_sel; ++j) {                // pass 2: dIQ += gz idx_k
+      for (int j = 0; ok && !kKeysDQ<G> && j < n_sel; ++j) { // pass 2: dIQ += gz idx_k
         const int rr = n_sel + j, st = rr & 1;
         if (!ptx::mbar_wait(&s.g_full[j & 1], (j >> 1) & 1, abort)) { ok = false; break; }
         ptx::tc_fence_after_sync();
@@ -389,6 +401,17 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       rec[r] = lse2;
       if (hh == 0) rec[kRows + r / G] = lseI2;
     }
+    if constexpr (kKeysDQ<G>) {
+      // d idx_q and the loss come from the key-block pass, which adds into d idx_q
+      if (!ok && lane == 0) raise_abort(&s.abort, status, 0x703);
+      if (valid && hh == 0) {
+        float4* dst = reinterpret_cast<float4*>(d_idx_q + (((size_t)b * p.Sq + t) * p.Hkv + g) * kD);
+#pragma unroll
+        for (int u = 0; u < kCols32; ++u)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) dst[(kCols32 * half + u) * 8 + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    } else {
     float lsum = 0.f;
     for (int j = 0; ok && j < n_sel; ++j) {
       const int lim = t - s.blocks[j] * kBk;
@@ -485,6 +508,7 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
     if (lane == 0 && lv != 0.f) atomicAdd(loss, lv);
+    }
   }
 
   ptx::tc_fence_before_sync();
@@ -505,6 +529,7 @@ struct __align__(1024) SmemK {
   uint8_t ik[kTileBytes];
   uint8_t q[2][kTileBytes];
   uint8_t iq[2][kIqBytes];
+  uint8_t gzs[2][2 * 16 * kRowBytes];   // gz (16 tokens x 128 keys, K-major) for d idx_q^T
   float rec[2][2 * kRows];     // a group's lse2 per row [0,128), lseI2 per token [128,..)
   uint64_t kv_full, g_full[2], g_empty[2];
   uint64_t s_full[2], p_full[2], acc_done[2], drain[2];   // per S^T / gz^T buffer
@@ -529,7 +554,8 @@ __global__ void __launch_bounds__(KeysWarps<G>::kThreads, 1)
 kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_ik, const __grid_constant__ CUtensorMap tm_iq,
                   const uint32_t* __restrict__ bits, const float* __restrict__ rowstat,
-                  float* __restrict__ d_idx_k, Dims p, int words,
+                  float* __restrict__ d_idx_k, float* __restrict__ d_idx_q,
+                  float* __restrict__ loss, Dims p, int words,
                   int words_per_cta, int* status) {
   extern __shared__ uint8_t smem_raw[];
   SmemK& s = *reinterpret_cast<SmemK*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -571,6 +597,9 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   using W = KeysWarps<G>;
   for (int i = threadIdx.x; i < 2 * kIqBytes / 16; i += W::kThreads)
     reinterpret_cast<uint4*>(&s.iq[0][0])[i] = make_uint4(0, 0, 0, 0);
+  // so do the gz rows past a group's tokens in the d idx_q^T operand
+  for (int i = threadIdx.x; i < (int)sizeof(s.gzs) / 16; i += W::kThreads)
+    reinterpret_cast<uint4*>(&s.gzs[0][0])[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     ptx::mbar_init(&s.kv_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -602,6 +631,9 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   // with 64 (G = 2) they are single: S^T 0, Z^T [128,192), gz^T [192,224).
   constexpr int kNBuf = kNTok <= 32 ? 2 : 1;
   constexpr uint32_t kColDK = 256;
+  // d idx_q^T of a group (index dims x its 16 token columns), per buffer (G >= 8 only)
+  auto col_dq = [](int b) -> uint32_t { return b == 0 ? 208u : 240u; };
+  constexpr uint32_t kIdescDQ = ptx::idesc_bf16_f32(128, 16, 1, 0);   // A (idx_k^T) MN-major
   auto col_s = [](int b) -> uint32_t { return b == 0 ? 0u : 384u; };
   auto col_z = [](int b) -> uint32_t { return b == 0 ? 128u : 160u; };
   auto col_g = [](int b) -> uint32_t { return b == 0 ? 192u : 224u; };
@@ -673,6 +705,17 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                               ptx::smem_desc_mn_sw128(ptx::smem_u32(s.iq[st]) + kk * 16 * kRowBytes,
                                                       kIqRows * kRowBytes, 1024),
                               kIdescMN, (gi > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (kKeysDQ<G>) {
+            // d idx_q^T = idx_k^T (index dims x keys: the block's idx_k tile read MN-major)
+            // gz^T (keys x tokens: gz K-major in shared memory)
+            const uint32_t gb = ptx::smem_u32(s.gzs[bf]);
+#pragma unroll
+            for (int kk = 0; kk < kBk / 16; ++kk)
+              ptx::umma_bf16_ss(tmem + col_dq(bf),
+                                ptx::smem_desc_mn_sw128(ia + kk * 16 * kRowBytes, kBk * kRowBytes, 1024),
+                                ptx::smem_desc_k_sw128(gb + (kk >> 2) * (16 * kRowBytes) + (kk & 3) * 32),
+                                kIdescDQ, kk > 0 ? 1u : 0u);
+          }
           ptx::umma_commit(&s.acc_done[bf]);
           ptx::umma_commit(&s.g_empty[st]);
         }
@@ -706,6 +749,25 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::tmem_st_wait();
     }
     bool ok = true;
+    float lsum = 0.f;                                         // this lane's loss terms (log2)
+    // d idx_q of group gd (its d idx_q^T MMA complete): this warp's tokens of it, this lane's
+    // index dimension, added to the output
+    auto flush_dq = [&](int gd) {
+      const int bq = gd % kNBuf;
+      const int md = s.tiles[gd / parts], pd = gd % parts;
+      const int td = md * kQt + pd * kTok;
+      uint32_t v[16];
+      ptx::tmem_ld_x16(tmem + lane_off + col_dq(bq), v);
+      ptx::tmem_ld_wait();
+      const int dim = quad * 32 + lane;
+      // the column index stays a compile-time constant (v in registers)
+#pragma unroll
+      for (int tok = 0; tok < kTok; ++tok) {
+        if (tok / kTokW == part_w && td + tok < p.Sq)
+          atomicAdd(d_idx_q + (((size_t)b * p.Sq + td + tok) * p.Hkv + g) * kD + dim,
+                    __uint_as_float(v[tok]) * p.index_scale);
+      }
+    };
     for (int gi = 0; gi < n_groups; ++gi) {
       const int st = gi & 1, bf = gi % kNBuf;
       const uint32_t ph = (gi / kNBuf) & 1;
@@ -716,6 +778,9 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // the d idx_k MMA of the group that last used this gz^T buffer has read it
           (gi >= kNBuf && !ptx::mbar_wait(&s.acc_done[bf], ph ^ 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
+      if constexpr (kKeysDQ<G>) {
+        if (gi >= kNBuf) flush_dq(gi - kNBuf);
+      }
       uint32_t sv[kCols32][32];
 #pragma unroll
       for (int u = 0; u < kCols32; ++u)
@@ -748,12 +813,28 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         for (int u = 0; u < 2; ++u) {
           const int tok = part_w * kTokW + tk + u;            // token of the group
           const bool vis = key <= t0 + tok && t0 + tok < p.Sq;
-          const float pi = vis ? ex2(fmaf(__uint_as_float(zv[(tk + u) / 16][(tk + u) % 16]), c2,
-                                          -s.rec[st][kRows + tok]))
-                               : 0.f;
-          gz2[u] = pi - pt[tk + u] * (1.f / G);
+          const float zl = fmaf(__uint_as_float(zv[(tk + u) / 16][(tk + u) % 16]), c2,
+                                -s.rec[st][kRows + tok]);      // log2 p_I
+          const float pi = vis ? ex2(zl) : 0.f;
+          const float ptm = pt[tk + u] * (1.f / G);
+          if constexpr (kKeysDQ<G>) {
+            if (ptm > 0.f) lsum += ptm * (__log2f(ptm) - zl);
+          }
+          gz2[u] = pi - ptm;
         }
         pk[tk >> 1] = pack_bf16x2(gz2[0], gz2[1]);
+        if constexpr (kKeysDQ<G>) {
+          // gz of this key for the two tokens, into the K-major operand of d idx_q^T: row =
+          // token, 16-byte unit (key % 64) / 8 swizzled with the row, chunk = key / 64
+          const int kl = quad * 32 + lane;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int n = part_w * kTokW + tk + u;
+            const uint32_t off = (kl >> 6) * (16 * kRowBytes) + n * kRowBytes +
+                                 ((((kl & 63) >> 3) ^ (n & 7)) << 4) + (kl & 7) * 2;
+            *reinterpret_cast<__nv_bfloat16*>(&s.gzs[bf][off]) = __float2bfloat16_rn(gz2[u]);
+          }
+        }
       }
       // this warp's tokens' gz^T columns (2 tokens per column)
       const uint32_t gcol = tmem + lane_off + col_g(bf) + part_w * (kTokW / 2);
@@ -763,11 +844,24 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       else if constexpr (kTokW / 2 == 8) ptx::tmem_st_x8(gcol, pk);
       else ptx::tmem_st_x16(gcol, pk);
       ptx::tmem_st_wait();
+      if constexpr (kKeysDQ<G>) ptx::fence_proxy_async_smem();   // gz for the tensor core
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s.p_full[bf]);
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x713);
+    if constexpr (kKeysDQ<G>) {
+      // the last groups' d idx_q (each buffer's last MMA, then its product)
+      for (int gd = n_groups > kNBuf ? n_groups - kNBuf : 0; ok && gd < n_groups; ++gd) {
+        if (!ptx::mbar_wait(&s.acc_done[gd % kNBuf], (gd / kNBuf) & 1, abort)) { ok = false; break; }
+        ptx::tc_fence_after_sync();
+        flush_dq(gd);
+      }
+      float lv = lsum * kLn2;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lv += __shfl_xor_sync(0xffffffffu, lv, o);
+      if (lane == 0 && lv != 0.f) atomicAdd(loss, lv);
+    }
     // the last d idx_k MMA (one issuing thread: it follows all the others)
     const bool have = ok && ptx::mbar_wait(&s.acc_done[(n_groups - 1) % kNBuf],
                                            ((n_groups - 1) / kNBuf) & 1, abort);
@@ -833,8 +927,8 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
     const int words = (p.nR + 31) / 32;
     const int wpc = tiles_per_cta(p) / 32;
     dim3 grid((words + wpc - 1) / wpc, p.nB, p.B * p.Hkv);
-    kern<<<grid, KeysWarps<G>::kThreads, smem, st>>>(tq, tk, tik, tiq, bits, rowstat, d_idx_k, p, words, wpc,
-                                       status);
+    kern<<<grid, KeysWarps<G>::kThreads, smem, st>>>(tq, tk, tik, tiq, bits, rowstat, d_idx_k,
+                                                     d_idx_q, loss, p, words, wpc, status);
     e = cudaGetLastError();
   }
   return e;
