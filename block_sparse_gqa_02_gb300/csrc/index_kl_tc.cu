@@ -753,19 +753,20 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // d idx_q of group gd (its d idx_q^T MMA complete): this warp's tokens of it, this lane's
     // index dimension, added to the output
     auto flush_dq = [&](int gd) {
-      const int bq = gd % kNBuf;
-      const int md = s.tiles[gd / parts], pd = gd % parts;
-      const int td = md * kQt + pd * kTok;
-      uint32_t v[16];
-      ptx::tmem_ld_x16(tmem + lane_off + col_dq(bq), v);
-      ptx::tmem_ld_wait();
-      const int dim = quad * 32 + lane;
-      // the column index stays a compile-time constant (v in registers)
+      if constexpr (kKeysDQ<G>) {
+        const int bq = gd % kNBuf;
+        const int md = s.tiles[gd / parts], pd = gd % parts;
+        const int td = md * kQt + pd * kTok;
+        static_assert(kTokW == 2 || kTokW == 4, "d idx_q columns per warp");
+        uint32_t v[kTokW];
+        if constexpr (kTokW == 4) ptx::tmem_ld_x4(tmem + lane_off + col_dq(bq) + part_w * kTokW, v);
+        else ptx::tmem_ld_x2(tmem + lane_off + col_dq(bq) + part_w * kTokW, v);
+        ptx::tmem_ld_wait();
+        const int tw = td + part_w * kTokW;                     // this warp's first token
+        float* dst = d_idx_q + (((size_t)b * p.Sq + tw) * p.Hkv + g) * kD + quad * 32 + lane;
 #pragma unroll
-      for (int tok = 0; tok < kTok; ++tok) {
-        if (tok / kTokW == part_w && td + tok < p.Sq)
-          atomicAdd(d_idx_q + (((size_t)b * p.Sq + td + tok) * p.Hkv + g) * kD + dim,
-                    __uint_as_float(v[tok]) * p.index_scale);
+        for (int x = 0; x < kTokW; ++x)
+          if (tw + x < p.Sq) atomicAdd(dst + (size_t)x * p.Hkv * kD, __uint_as_float(v[x]) * p.index_scale);
       }
     };
     for (int gi = 0; gi < n_groups; ++gi) {
