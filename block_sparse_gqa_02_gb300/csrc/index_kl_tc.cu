@@ -519,6 +519,261 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   }
 }
 
+// ============================================================== normaliser kernel (G >= 8)
+// The index log-normaliser lseI2 of every token over the visible keys of its tile's
+// selection, with the tokens themselves as the MMA's 128 rows: a CTA takes two consecutive
+// 64-query tiles of one (sequence, KV head) and walks the union of their selections; a row
+// skips the blocks its own tile did not select.  Each token's index query is used once (the
+// query-tile form repeats it over the G rows of its heads).  Writes each 128-row group's
+// record for the key-block pass (lse2 per row, lseI2 per token) and zeroes d idx_q.
+
+// An even number of stages: stage u % kNormStages is always read by issuer u % 2, so each
+// issuer waits for a stage's phases in order (with an odd count a stage's consecutive
+// phases alternate between the issuers, and a parity wait could pass a phase early).
+constexpr int kNormStages = 4;
+constexpr int kNormMaxU = 2 * kMaxSel;
+constexpr int kNormMath = 16;                                // four per TMEM lane quadrant
+constexpr int kNormProducer = kNormMath, kNormMma = kNormMath + 1;   // issuers: 17, 18
+constexpr int kNormThreads = (kNormMath + 3) * 32;
+constexpr uint32_t kNormTmemCols = 256;
+
+struct __align__(1024) SmemN {
+  uint8_t iq[kTileBytes];                 // idx_q of the 128 tokens (K-major, 128-byte swizzle)
+  uint8_t ik[kNormStages][kTileBytes];
+  uint64_t iq_full, ring_full[kNormStages], ring_empty[kNormStages];
+  uint64_t z_full[2], z_free[2], drain[2];
+  float part_ml[4][2][kRows];             // [column part][max, sum][token]
+  int ublk[kNormMaxU];                    // the union, first tile's blocks first
+  int umask[kNormMaxU];                   // bit 0: the first tile selected it, bit 1: the second
+  int n_u;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int G>
+__global__ void __launch_bounds__(kNormThreads, 1)
+kl_norm_tc_kernel(const __grid_constant__ CUtensorMap tm_ik, const __grid_constant__ CUtensorMap tm_iq,
+                  const int32_t* __restrict__ sel, const float* __restrict__ lse,
+                  float* __restrict__ rowstat, float* __restrict__ d_idx_q, Dims p, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  SmemN& s = *reinterpret_cast<SmemN*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                       ~uintptr_t(1023));
+  constexpr int kTok = kRows / G;                             // tokens of a 128-row group
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = 2 * (gridDim.x - 1 - blockIdx.x);            // later tiles first
+  const int bg = blockIdx.y, b = bg / p.Hkv, g = bg % p.Hkv;
+  const int parts = p.Qt * G / kRows;                         // 128-row groups per tile
+  const volatile int* abort = &s.abort;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&s.iq_full, 1);
+    for (int i = 0; i < kNormStages; ++i) {
+      ptx::mbar_init(&s.ring_full[i], 1);
+      ptx::mbar_init(&s.ring_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.z_full[i], 1);
+      ptx::mbar_init(&s.z_free[i], kNormMath);
+      ptx::mbar_init(&s.drain[i], 1);
+    }
+    s.abort = 0;
+    ptx::fence_barrier_init();
+    if (p.inject != 1) {                                      // test hook: no copies at all
+      ptx::tma_prefetch_desc(&tm_iq);
+      ptx::mbar_arrive_expect_tx(&s.iq_full, kTileBytes);
+      debug_check(m0 < p.nR && bg < p.B * p.Hkv, status, kDbgCoord);
+      for (int kc = 0; kc < 2; ++kc)
+        ptx::tma_load_4d(s.iq + kc * kRows * kRowBytes, &tm_iq, &s.iq_full, kc * 64, g,
+                         m0 * kQt, b);
+    }
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(&s.tmem_base, kNormTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 1) {
+    // the union of the two tiles' selections (entries < 0 or >= nB are skipped)
+    const int32_t* row0 = sel + ((size_t)bg * p.nR + m0) * p.k;
+    int n = 0;
+    for (int i0 = 0; i0 < p.k; i0 += 32) {
+      const int i = i0 + lane;
+      const int blk = i < p.k ? row0[i] : -1;
+      const bool ok = blk >= 0 && blk < p.nB;
+      const unsigned mask = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        const int at = n + __popc(mask & ((1u << lane) - 1));
+        s.ublk[at] = blk;
+        s.umask[at] = 1;
+      }
+      n += __popc(mask);
+    }
+    __syncwarp();
+    const int n0 = n;
+    if (m0 + 1 < p.nR) {
+      const int32_t* row1 = row0 + p.k;
+      for (int i0 = 0; i0 < p.k; i0 += 32) {
+        const int i = i0 + lane;
+        const int blk = i < p.k ? row1[i] : -1;
+        bool add = blk >= 0 && blk < p.nB;
+        if (add) {
+          for (int j = 0; j < n0; ++j)
+            if (s.ublk[j] == blk) {                           // selected by both tiles
+              atomicOr(&s.umask[j], 2);
+              add = false;
+              break;
+            }
+        }
+        const unsigned mask = __ballot_sync(0xffffffffu, add);
+        if (add) {
+          const int at = n + __popc(mask & ((1u << lane) - 1));
+          s.ublk[at] = blk;
+          s.umask[at] = 2;
+        }
+        n += __popc(mask);
+      }
+    }
+    if (lane == 0) s.n_u = n;
+  }
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem = s.tmem_base;
+  const int n_u = s.n_u;
+
+  if (warp == kNormProducer) {
+    int issued = 0;
+    bool ok = true;
+    const int n_load = p.inject == 1 ? 0 : n_u;
+    if (lane == 0 && n_load > 0) ptx::tma_prefetch_desc(&tm_ik);
+    for (int u = 0; u < n_load; ++u) {
+      const int st = u % kNormStages;
+      if (!ptx::mbar_wait(&s.ring_empty[st], ((u / kNormStages) & 1) ^ 1, abort)) { ok = false; break; }
+      if (lane == 0) {
+        const int blk = s.ublk[u];
+        debug_check(blk >= 0 && blk < p.nB, status, kDbgCoord);
+        ptx::mbar_arrive_expect_tx(&s.ring_full[st], kTileBytes);
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_3d(s.ik[st] + kc * kBk * kRowBytes, &tm_ik, &s.ring_full[st], kc * 64,
+                           blk * kBk, b);
+      }
+      issued = u + 1;
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x721);
+    if (*abort && lane == 0 && p.inject != 1) {
+      if (n_u > 0) ptx::mbar_wait_timed(&s.iq_full, 0);
+      for (int u = issued > kNormStages ? issued - kNormStages : 0; u < issued; ++u)
+        ptx::mbar_wait_timed(&s.ring_full[u % kNormStages], (u / kNormStages) & 1);
+    }
+  } else if (warp == kNormMma || warp == kNormMma + 1) {
+    // the two issuers take alternate blocks, each into its own Z buffer
+    const int who = warp - kNormMma;
+    bool ok = n_u > 0 ? ptx::mbar_wait(&s.iq_full, 0, abort) : true;
+    bool issued_any = false;
+    const uint32_t qa = ptx::smem_u32(s.iq);
+    for (int u = who; ok && u < n_u; u += 2) {
+      const int st = u % kNormStages, buf = u & 1;
+      if (!ptx::mbar_wait(&s.ring_full[st], (u / kNormStages) & 1, abort) ||
+          (u >= 2 && !ptx::mbar_wait(&s.z_free[buf], ((u >> 1) & 1) ^ 1, abort))) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      if (lane == 0) {
+        mma_kk(tmem + buf * 128, qa, ptx::smem_u32(s.ik[st]), kBk * kRowBytes, kIdescKK);
+        ptx::umma_commit(&s.z_full[buf]);
+        ptx::umma_commit(&s.ring_empty[st]);
+      }
+      issued_any = true;
+      __syncwarp();
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x722);
+    if (*abort && lane == 0 && issued_any) {
+      ptx::umma_commit(&s.drain[who]);
+      ptx::mbar_wait_timed(&s.drain[who], 0);
+    }
+  } else {
+    // ------------------ math warps: warp w takes tokens 32 (w % 4) .. +31 (a TMEM lane
+    // quadrant; quadrants 0-1 are the first tile, 2-3 the second) and key columns
+    // 32 (w / 4) .. +31 of every block
+    const int quad = warp & 3, part_w = warp >> 2;
+    const int r = quad * 32 + lane;                           // token row of the CTA
+    const int t = m0 * kQt + r;
+    const int tile_bit = quad < 2 ? 1 : 2;
+    const float c2 = p.index_scale * kLog2e;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    float mI = -INFINITY, lI = 0.f;
+    bool ok = true;
+    for (int u = 0; u < n_u; ++u) {
+      const int buf = u & 1;
+      if (!ptx::mbar_wait(&s.z_full[buf], (u >> 1) & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      uint32_t zv[32];
+      ptx::tmem_ld_x32(tmem + lane_off + buf * 128 + part_w * 32, zv);
+      ptx::tmem_ld_wait();
+      ptx::tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&s.z_free[buf]);
+      if (s.umask[u] & tile_bit) {                            // the same in the whole warp
+        const int lim = t - s.ublk[u] * kBk - part_w * 32;    // visible columns: c <= lim
+        float zk[32];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          zk[c] = c <= lim ? __uint_as_float(zv[c]) * c2 : -INFINITY;
+          cm = fmaxf(cm, zk[c]);
+        }
+        if (cm != -INFINITY) {
+          const float mn = fmaxf(mI, cm);
+          float acc = 0.f;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) acc += ex2(zk[c] - mn);
+          lI = lI * ex2(mI - mn) + acc;
+          mI = mn;
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_abort(&s.abort, status, 0x723);
+    // every math warp reaches this barrier exactly once (also after a failed wait)
+    s.part_ml[part_w][0][r] = mI;
+    s.part_ml[part_w][1][r] = lI;
+    asm volatile("bar.sync 1, %0;" ::"r"(kNormMath * 32) : "memory");
+    mI = -INFINITY;
+    lI = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float mo = s.part_ml[q][0][r], lo = s.part_ml[q][1][r];
+      const float mn = fmaxf(mI, mo);
+      if (mn != -INFINITY) {
+        lI = lI * ex2(mI - mn) + lo * ex2(mo - mn);
+        mI = mn;
+      }
+    }
+    const float lseI2 = mI == -INFINITY ? -INFINITY : mI + __log2f(lI);
+    // the token's entries of its group's record: lse2 of its G rows, then lseI2
+    const int mt = m0 + (r >> 6), it = r & 63;
+    const bool valid = t < p.Sq;
+    if (mt < p.nR) {
+      const int grp = it / kTok, tok = it % kTok;
+      float* rec = rowstat + (((size_t)bg * p.nR + mt) * parts + grp) * 2 * kRows;
+      if (part_w == 0) rec[kRows + tok] = lseI2;
+      for (int hh = part_w; hh < G; hh += 4)
+        rec[tok * G + hh] = valid ? lse[((size_t)b * p.Hq + g * G + hh) * p.Sq + t] * kLog2e
+                                  : INFINITY;
+    }
+    if (valid) {
+      // d idx_q is added into by the key-block pass
+      float4* dst = reinterpret_cast<float4*>(d_idx_q + (((size_t)b * p.Sq + t) * p.Hkv + g) * kD);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dst[part_w * 8 + e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem, kNormTmemCols);
+  }
+}
+
 // ===================================================================== keys kernel
 
 constexpr int kIqRows = 64;                                   // idx_q rows of a group, padded
@@ -910,7 +1165,20 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
   const uint32_t qb[4] = {64, 1, (uint32_t)(kRows / G), 1};
   cudaError_t e = make_tensor_map_bf16(&tiq, idx_q, 4, qd, qs, qb);
   if (e != cudaSuccess) return e;
-  {
+  if constexpr (kKeysDQ<G>) {
+    // idx_q as (dI, Hkv, T, B) with one box = 64 dims x 1 head x 128 tokens (two tiles)
+    CUtensorMap tiq128;
+    const uint32_t qb128[4] = {64, 1, (uint32_t)kRows, 1};
+    e = make_tensor_map_bf16(&tiq128, idx_q, 4, qd, qs, qb128);
+    if (e != cudaSuccess) return e;
+    auto kern = kl_norm_tc_kernel<G>;
+    const size_t smem = sizeof(SmemN) + 1024;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.nR + 1) / 2, p.B * p.Hkv);
+    kern<<<grid, kNormThreads, smem, st>>>(tik, tiq128, sel, lse, rowstat, d_idx_q, p, status);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
     auto kern = kl_rows_tc_kernel<G>;
     const size_t smem = sizeof(SmemR) + 1024;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
