@@ -555,8 +555,8 @@ def backward_32k(args, device, stream, flush, tc_peak):
             "index_kl": {"ms": kl_ms, "algorithmic_flops": f_kl,
                          "tflops": f_kl / (kl_ms / 1e3) / 1e12,
                          "frac_of_tensor_peak": f_kl / (kl_ms / 1e3) / 1e12 / tc_peak,
-                         "kernel": "tcgen05: query-tile pass (index normaliser), key-block "
-                                   "pass (loss, d idx_q, d idx_k) for G >= 8"}}
+                         "kernel": "tcgen05: normaliser pass (two query tiles per CTA), "
+                                   "key-block pass (loss, d idx_q, d idx_k) for G >= 8"}}
 
 
 def cpu_baseline_prefill(cfg, host, budget_s=15.0, seed=0):

@@ -11,15 +11,19 @@
 //   loss += sum_j p_T (ln p_T - ln p_I);  gz_j = p_I - p_T = dloss / d(index_scale z_j)
 //   d idx_q[t,g] = index_scale sum_j gz_j idx_k[j];  d idx_k[j] += index_scale gz_j idx_q[t,g].
 //
-// Two kernels:
-// * rows (query-tile order, one CTA per 128 (token, head) rows like the forward): a pass
-//   over the blocks forms lseI2 from Z = idx_q idx_k^T, with each row's idx_q replicated so
-//   that every row of a token holds its token's index logits, and leaves each 128-row
-//   group's main lse2 (per row) and lseI2 (per token) as one 1 KiB record.  With G < 8 a
-//   second pass forms S and Z again (S into one of two TMEM buffers, so a block's S and Z
-//   are computed while the math warps work on the previous block), the math warps average
-//   the G rows of a token with warp shuffles, accumulate the loss and write gz into TMEM,
-//   and d idx_q += gz idx_k accumulates in TMEM.  With G >= 8 it only zeroes d idx_q.
+// Kernels:
+// * norm (G >= 8; one CTA per two consecutive 64-query tiles of a (sequence, KV head)): the
+//   index log-normaliser lseI2 of every token, with the 128 tokens as the rows of
+//   Z = idx_q idx_k^T over the union of the two tiles' selections; it writes each 128-row
+//   group's record for the key-block pass (the main branch's lse2 per row, lseI2 per token)
+//   and zeroes d idx_q.
+// * rows (G < 8; query-tile order, one CTA per 128 (token, head) rows like the forward): a
+//   first walk forms lseI2 from Z with each row's idx_q replicated so that every row of a
+//   token holds its token's index logits, and writes the same record; a second walk forms S
+//   and Z again (S into one of two TMEM buffers, so a block's S and Z are computed while the
+//   math warps work on the previous block), the math warps average the G rows of a token
+//   with warp shuffles, accumulate the loss and write gz into TMEM, and d idx_q += gz idx_k
+//   accumulates in TMEM.
 // * keys (key-block order over the tiles that selected the block, as in the dK/dV pass of
 //   the backward): S^T = K Q^T and Z^T = idx_k idx_q^T with the keys on the TMEM lanes, so a
 //   token's G rows are adjacent columns; gz^T goes to TMEM and d idx_k += gz^T idx_q
@@ -27,8 +31,7 @@
 //   G >= 8 (at most 16 tokens a group) it also forms the loss terms and, per group,
 //   d idx_q^T = idx_k^T gz^T (the block's idx_k tile read MN-major, gz written K-major to
 //   shared memory) into 16 TMEM columns, which the math warps add into d idx_q with fp32
-//   atomics two groups later: the second walk of the query-tile pass, which repeated the
-//   block products the key-block pass forms anyway, is gone (32K: 4.23 -> 2.87 ms).
+//   atomics two groups later.
 // Warps: 16 elementwise warps (four per TMEM lane quadrant, each taking a quarter of the
 // columns; 8 for G = 32, where a thread needs more registers than 608 threads leave), a TMA
 // producer and two MMA issuers (a single thread's stream of N = 128 MMAs with commits in it
