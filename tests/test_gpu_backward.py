@@ -74,6 +74,11 @@ KL_CASES = {
     "bf16_g32_ragged": CONFIGS["p32k"].with_(seq=900, n_heads_q=128, top_k=3, n_plants=0),
     "bf16_g64_ragged": CONFIGS["p32k"].with_(seq=500, n_heads_q=256, top_k=3, n_plants=0),
     "bf16_8192_k32": CONFIGS["p32k"].with_(seq=8192, top_k=32, n_plants=4),
+    # the normaliser pass (G >= 8) takes two tiles per CTA over the union of their
+    # selections: k = 1 (the two tiles of a block share their current block) with an odd
+    # tile count (the last CTA holds one tile), and a wider union at G = 16
+    "bf16_g8_k1_odd_tiles": CONFIGS["p32k"].with_(seq=1300, top_k=1, n_plants=0),
+    "bf16_g16_k24": CONFIGS["p32k"].with_(seq=2000, n_heads_q=64, top_k=24, n_plants=2),
     "bf16_b2_ragged": CONFIGS["p32k"].with_(batch=2, seq=1100, top_k=4, n_plants=2),
 }
 
