@@ -1009,22 +1009,26 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     bool ok = true;
     float lsum = 0.f;                                         // this lane's loss terms (log2)
     // d idx_q of group gd (its d idx_q^T MMA complete): this warp's tokens of it, this lane's
-    // index dimension, added to the output
-    auto flush_dq = [&](int gd) {
+    // index dimension.  dq_load issues the TMEM load (waited for with the caller's other
+    // loads), dq_add adds the values into the output.
+    constexpr int kTokQ = kTokW == 2 || kTokW == 4 ? kTokW : 2;
+    uint32_t dqv[kTokQ];
+    auto dq_load = [&](int gd) {
       if constexpr (kKeysDQ<G>) {
-        const int bq = gd % kNBuf;
-        const int md = s.tiles[gd / parts], pd = gd % parts;
-        const int td = md * kQt + pd * kTok;
         static_assert(kTokW == 2 || kTokW == 4, "d idx_q columns per warp");
-        uint32_t v[kTokW];
-        if constexpr (kTokW == 4) ptx::tmem_ld_x4(tmem + lane_off + col_dq(bq) + part_w * kTokW, v);
-        else ptx::tmem_ld_x2(tmem + lane_off + col_dq(bq) + part_w * kTokW, v);
-        ptx::tmem_ld_wait();
-        const int tw = td + part_w * kTokW;                     // this warp's first token
+        const uint32_t a = tmem + lane_off + col_dq(gd % kNBuf) + part_w * kTokW;
+        if constexpr (kTokW == 4) ptx::tmem_ld_x4(a, dqv);
+        else ptx::tmem_ld_x2(a, dqv);
+      }
+    };
+    auto dq_add = [&](int gd) {
+      if constexpr (kKeysDQ<G>) {
+        const int md = s.tiles[gd / parts], pd = gd % parts;
+        const int tw = md * kQt + pd * kTok + part_w * kTokW;   // this warp's first token
         float* dst = d_idx_q + (((size_t)b * p.Sq + tw) * p.Hkv + g) * kD + quad * 32 + lane;
 #pragma unroll
         for (int x = 0; x < kTokW; ++x)
-          if (tw + x < p.Sq) atomicAdd(dst + (size_t)x * p.Hkv * kD, __uint_as_float(v[x]) * p.index_scale);
+          if (tw + x < p.Sq) atomicAdd(dst + (size_t)x * p.Hkv * kD, __uint_as_float(dqv[x]) * p.index_scale);
       }
     };
     for (int gi = 0; gi < n_groups; ++gi) {
@@ -1037,9 +1041,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           // the d idx_k MMA of the group that last used this gz^T buffer has read it
           (gi >= kNBuf && !ptx::mbar_wait(&s.acc_done[bf], ph ^ 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      if constexpr (kKeysDQ<G>) {
-        if (gi >= kNBuf) flush_dq(gi - kNBuf);
-      }
+      const bool have_dq = kKeysDQ<G> && gi >= kNBuf;
+      if (have_dq) dq_load(gi - kNBuf);
       uint32_t sv[kCols32][32];
 #pragma unroll
       for (int u = 0; u < kCols32; ++u)
@@ -1052,6 +1055,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int c = 0; c < kZLoads; ++c)
         ptx::tmem_ld_x16(tmem + lane_off + col_z(bf) + part_w * kTokW + c * 16, zv[c]);
       ptx::tmem_ld_wait();
+      if (have_dq) dq_add(gi - kNBuf);
       float pt[kTokW];
 #pragma unroll
       for (int x = 0; x < kTokW; ++x) pt[x] = 0.f;
@@ -1114,7 +1118,9 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       for (int gd = n_groups > kNBuf ? n_groups - kNBuf : 0; ok && gd < n_groups; ++gd) {
         if (!ptx::mbar_wait(&s.acc_done[gd % kNBuf], (gd / kNBuf) & 1, abort)) { ok = false; break; }
         ptx::tc_fence_after_sync();
-        flush_dq(gd);
+        dq_load(gd);
+        ptx::tmem_ld_wait();
+        dq_add(gd);
       }
       float lv = lsum * kLn2;
 #pragma unroll
