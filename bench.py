@@ -678,8 +678,9 @@ def run_ours(args, rank, world, device):
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": pre_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{pcfg.name}: {pcfg.description}"
-                               + (f" | decode {dcfg.name}: {dcfg.description}" if dec else ""),
+        # the headline workload (the one `value` measures, and the reference arm's); the
+        # decode leg names its own inside "decode"
+        "config": {"workload": f"{pcfg.name}: {pcfg.description}",
                    "global_batch": pcfg.batch * world, "seq_len": pcfg.seq,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
                    "l2": "flushed by a 256 MiB write before every timed kernel sequence",
