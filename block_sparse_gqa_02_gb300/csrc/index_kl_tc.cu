@@ -74,6 +74,26 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (one 64-bit register) for the paired FMA / ADD instructions.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void split_f32x2(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -399,10 +419,11 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // operand, so the rows of a token hold partial d idx_q that are summed at the end.
     const float lse2 = valid ? lse[((size_t)b * p.Hq + h) * p.Sq + t] * kLog2e : INFINITY;
     if (half == 0) {
-      // the group's record for the key-block pass: lse2 per row, then lseI2 per token
+      // the group's record for the key-block pass: -lse2 per row, then -lseI2 per token
+      // (negated, so that the key-block pass adds them in a paired FMA)
       float* rec = rowstat + (((size_t)bg * p.nR + m) * gridDim.x + part) * 2 * kRows;
-      rec[r] = lse2;
-      if (hh == 0) rec[kRows + r / G] = lseI2;
+      rec[r] = -lse2;
+      if (hh == 0) rec[kRows + r / G] = -lseI2;
     }
     if constexpr (kKeysDQ<G>) {
       // d idx_q and the loss come from the key-block pass, which adds into d idx_q
@@ -750,16 +771,17 @@ kl_norm_tc_kernel(const __grid_constant__ CUtensorMap tm_ik, const __grid_consta
       }
     }
     const float lseI2 = mI == -INFINITY ? -INFINITY : mI + __log2f(lI);
-    // the token's entries of its group's record: lse2 of its G rows, then lseI2
+    // the token's entries of its group's record (negated, as the key-block pass reads them):
+    // -lse2 of its G rows, then -lseI2
     const int mt = m0 + (r >> 6), it = r & 63;
     const bool valid = t < p.Sq;
     if (mt < p.nR) {
       const int grp = it / kTok, tok = it % kTok;
       float* rec = rowstat + (((size_t)bg * p.nR + mt) * parts + grp) * 2 * kRows;
-      if (part_w == 0) rec[kRows + tok] = lseI2;
+      if (part_w == 0) rec[kRows + tok] = -lseI2;
       for (int hh = part_w; hh < G; hh += 4)
-        rec[tok * G + hh] = valid ? lse[((size_t)b * p.Hq + g * G + hh) * p.Sq + t] * kLog2e
-                                  : INFINITY;
+        rec[tok * G + hh] = valid ? -lse[((size_t)b * p.Hq + g * G + hh) * p.Sq + t] * kLog2e
+                                  : -INFINITY;
     }
     if (valid) {
       // d idx_q is added into by the key-block pass
@@ -788,7 +810,7 @@ struct __align__(1024) SmemK {
   uint8_t q[2][kTileBytes];
   uint8_t iq[2][kIqBytes];
   uint8_t gzs[2][2 * 16 * kRowBytes];   // gz (16 tokens x 128 keys, K-major) for d idx_q^T
-  float rec[2][2 * kRows];     // a group's lse2 per row [0,128), lseI2 per token [128,..)
+  float rec[2][2 * kRows];     // a group's -lse2 per row [0,128), -lseI2 per token [128,..)
   uint64_t kv_full, g_full[2], g_empty[2];
   uint64_t s_full[2], p_full[2], acc_done[2], drain[2];   // per S^T / gz^T buffer
   int tiles[kMaxTilesPerCta];
@@ -1056,18 +1078,34 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ptx::tmem_ld_x16(tmem + lane_off + col_z(bf) + part_w * kTokW + c * 16, zv[c]);
       ptx::tmem_ld_wait();
       if (have_dq) dq_add(gi - kNBuf);
+      // the target: per token, the sum over its G rows (adjacent columns) of
+      // 2^(c1 s - lse2), two rows at a time in paired fp32 (G >= 2: a pair is one token's)
       float pt[kTokW];
+      {
+        const uint64_t c1x2 = f32x2(c1, c1);
+        uint64_t acc[kTokW];
 #pragma unroll
-      for (int x = 0; x < kTokW; ++x) pt[x] = 0.f;
+        for (int x = 0; x < kTokW; ++x) acc[x] = f32x2(0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < kCols32; ++u)
+        for (int u = 0; u < kCols32; ++u)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int x = part_w * kRowsW + u * 32 + e;        // row of the group
-          const int tok = (u * 32 + e) / G;                  // this warp's token index
-          if (key <= t0 + part_w * kTokW + tok)
-            pt[tok] += ex2(fmaf(__uint_as_float(sv[u][e]), c1, -s.rec[st][x]));
+          for (int e = 0; e < 32; e += 2) {
+            const int x = part_w * kRowsW + u * 32 + e;      // row of the group
+            const int tok = (u * 32 + e) / G;                // this warp's token index
+            const uint64_t nl = *reinterpret_cast<const uint64_t*>(&s.rec[st][x]);   // -lse2 pair
+            const uint64_t y = fma_f32x2(f32x2(__uint_as_float(sv[u][e]), __uint_as_float(sv[u][e + 1])),
+                                         c1x2, nl);
+            float y0, y1;
+            split_f32x2(y, y0, y1);
+            if (key <= t0 + part_w * kTokW + tok) acc[tok] = add_f32x2(acc[tok], f32x2(ex2(y0), ex2(y1)));
+          }
+#pragma unroll
+        for (int x = 0; x < kTokW; ++x) {
+          float a0, a1;
+          split_f32x2(acc[x], a0, a1);
+          pt[x] = a0 + a1;
         }
+      }
       uint32_t pk[kTokW / 2 > 0 ? kTokW / 2 : 1];
 #pragma unroll
       for (int tk = 0; tk < kTokW; tk += 2) {
@@ -1077,7 +1115,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           const int tok = part_w * kTokW + tk + u;            // token of the group
           const bool vis = key <= t0 + tok && t0 + tok < p.Sq;
           const float zl = fmaf(__uint_as_float(zv[(tk + u) / 16][(tk + u) % 16]), c2,
-                                -s.rec[st][kRows + tok]);      // log2 p_I
+                                s.rec[st][kRows + tok]);       // log2 p_I
           const float pi = vis ? ex2(zl) : 0.f;
           const float ptm = pt[tk + u] * (1.f / G);
           if constexpr (kKeysDQ<G>) {
