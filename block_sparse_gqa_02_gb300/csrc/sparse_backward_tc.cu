@@ -57,6 +57,31 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (one 64-bit register) for the paired FMA / ADD / MUL instructions.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void split_f32x2(uint64_t x, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -304,8 +329,8 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     if (half == 0) {
       // the group's record for the dK/dV pass: lse2 of its 128 rows, then their D
       float* rec = rowstat + (((size_t)bg * p.nR + m) * gridDim.x + part) * 2 * kRows;
-      rec[r] = lse2;
-      rec[kRows + r] = dsum;
+      rec[r] = -lse2;                                    // negated: the dK/dV pass adds them
+      rec[kRows + r] = -dsum;
     }
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     bool ok = true;
@@ -331,17 +356,20 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int u = 0; u < 1; ++u) {
         const int c = half + u;
         uint32_t pk[16];
+        const uint64_t c1x2 = f32x2(c1, c1), nl2 = f32x2(-lse2, -lse2), nd2 = f32x2(-dsum, -dsum);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float ds2[2];
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const float pr = c * 32 + e + w <= lim
-                                 ? ex2(fmaf(__uint_as_float(sv[u][e + w]), c1, -lse2))
-                                 : 0.f;
-            ds2[w] = pr * (__uint_as_float(dv[u][e + w]) - dsum);
-          }
-          pk[e >> 1] = pack_bf16x2(ds2[0], ds2[1]);
+          // two columns at a time in paired fp32
+          float y0, y1;
+          split_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[u][e]), __uint_as_float(sv[u][e + 1])),
+                                c1x2, nl2), y0, y1);
+          const float p0 = c * 32 + e <= lim ? ex2(y0) : 0.f;
+          const float p1 = c * 32 + e + 1 <= lim ? ex2(y1) : 0.f;
+          float d0, d1;
+          split_f32x2(mul_f32x2(f32x2(p0, p1),
+                                add_f32x2(f32x2(__uint_as_float(dv[u][e]), __uint_as_float(dv[u][e + 1])), nd2)),
+                      d0, d1);
+          pk[e >> 1] = pack_bf16x2(d0, d1);
         }
         ptx::tmem_st_x16(tmem + lane_off + kColDS + c * 16, pk);
       }
@@ -393,7 +421,7 @@ struct __align__(1024) SmemKV {
   uint8_t v[kTileBytes];
   uint8_t q[2][kTileBytes];
   uint8_t dO[2][kTileBytes];
-  float rec[2][2 * kRows];       // a group's lse2 [0,128) and D [128,256), per stage
+  float rec[2][2 * kRows];       // a group's -lse2 [0,128) and -D [128,256), per stage
   uint64_t kv_full, g_full[2], g_empty[2];
   uint64_t s_full, p_full, acc_dk, acc_dv, drain[2];
   int tiles[kMaxTilesPerCta];
@@ -582,17 +610,24 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int u = 0; u < 1; ++u) {
         const int c = half + u;
         uint32_t pp[16], dd[16];
+        const uint64_t c1x2 = f32x2(c1, c1);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float pr[2], dsv[2];
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const int x = c * 32 + e + w;
-            pr[w] = x >= xlim ? ex2(fmaf(__uint_as_float(sv[u][e + w]), c1, -s.rec[st][x])) : 0.f;
-            dsv[w] = pr[w] * (__uint_as_float(dpv[u][e + w]) - s.rec[st][kRows + x]);
-          }
-          pp[e >> 1] = pack_bf16x2(pr[0], pr[1]);
-          dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+          // two rows at a time in paired fp32; the record holds -lse2 and -D
+          const int x = c * 32 + e;
+          const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(&s.rec[st][x]);
+          const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(&s.rec[st][kRows + x]);
+          float y0, y1;
+          split_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[u][e]), __uint_as_float(sv[u][e + 1])),
+                                c1x2, nl2), y0, y1);
+          const float p0 = x >= xlim ? ex2(y0) : 0.f;
+          const float p1 = x + 1 >= xlim ? ex2(y1) : 0.f;
+          float d0, d1;
+          split_f32x2(mul_f32x2(f32x2(p0, p1),
+                                add_f32x2(f32x2(__uint_as_float(dpv[u][e]), __uint_as_float(dpv[u][e + 1])), nd2)),
+                      d0, d1);
+          pp[e >> 1] = pack_bf16x2(p0, p1);
+          dd[e >> 1] = pack_bf16x2(d0, d1);
         }
         // P^T / dS^T over columns this warp loaded: chunk c at columns 32c .. 32c+15
         ptx::tmem_st_x16(tmem + lane_off + kColS + 32 * c, pp);
