@@ -18,8 +18,9 @@
 // * dK, dV (key-outer, one CTA per (sequence, KV head, key block, range of query tiles)):
 //   the tiles that selected the block are read from a bitmap built first; for every 128-row
 //   group of those tiles S^T = K Q^T and dP^T = V dO^T go to TMEM (keys on the TMEM lanes),
-//   the elementwise warps form P^T and dS^T there, and dV += P^T dO, dK += dS^T Q accumulate
-//   in TMEM over all of the CTA's groups.  A CTA adds its dK / dV to the fp32 outputs with
+//   the elementwise warps form P^T there and release it (so dV += P^T dO, and the next
+//   group's S^T, run while they go on), then dS^T (dK += dS^T Q); dK and dV accumulate in
+//   TMEM over all of the CTA's groups.  A CTA adds its dK / dV to the fp32 outputs with
 //   vector atomics (a heavily selected block is split over several CTAs).
 // Warps: 16 elementwise warps (four per TMEM lane quadrant, each taking a quarter of the
 // columns of S / dP or S^T / dP^T: with two, the warps waited mostly on the latency of their
@@ -423,7 +424,7 @@ struct __align__(1024) SmemKV {
   uint8_t dO[2][kTileBytes];
   float rec[2][2 * kRows];       // a group's -lse2 [0,128) and -D [128,256), per stage
   uint64_t kv_full, g_full[2], g_empty[2];
-  uint64_t s_full, p_full, acc_dk, acc_dv, drain[2];
+  uint64_t s_full_s, s_full_dp, p_full_p, p_full_ds, acc_dk, acc_dv, drain[2];
   int tiles[kMaxTilesPerCta];
   int n_tiles;
   uint32_t tmem_base;
@@ -482,8 +483,10 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       ptx::mbar_init(&s.g_full[i], 1);
       ptx::mbar_init(&s.g_empty[i], 2);   // both issuers' MMAs read the group
     }
-    ptx::mbar_init(&s.s_full, 2);           // S^T from one issuer, dP^T from the other
-    ptx::mbar_init(&s.p_full, kMathWarps);
+    ptx::mbar_init(&s.s_full_s, 1);         // S^T landed
+    ptx::mbar_init(&s.s_full_dp, 1);        // dP^T landed
+    ptx::mbar_init(&s.p_full_p, kMathWarps);    // P^T written
+    ptx::mbar_init(&s.p_full_ds, kMathWarps);   // dS^T written
     ptx::mbar_init(&s.acc_dk, 1);
     ptx::mbar_init(&s.acc_dv, 1);
     ptx::mbar_init(&s.drain[0], 1);
@@ -545,31 +548,35 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     // ------------------------------------------------------------- MMA issuers
     // the first issuer: S^T = K Q^T, then dK += dS^T Q; the second: dP^T = V dO^T, then
     // dV += P^T dO.
-    // P^T is written over S^T and read by dV, dS^T over dP^T and read by dK, so each
-    // issuer's next product waits for the other issuer's last one, never for its own.
+    // P^T is written over S^T and read by dV, dS^T over dP^T and read by dK.  The first
+    // issuer takes the S region (S^T, then dV once P^T is written), the second the dP
+    // region (dP^T, then dK once dS^T is written): the math warps release P^T before they
+    // form dS^T, so dV and the next group's S^T run while dS^T is being formed.  Each
+    // issuer's next product overwrites what its own last one read, so it waits for that one.
     const int who = warp - kMmaWarp;
     bool ok = ptx::mbar_wait(&s.kv_full, 0, abort);
     bool issued_any = false;
     const uint32_t ka = ptx::smem_u32(s.k), va = ptx::smem_u32(s.v);
-    uint64_t* my_acc = who == 0 ? &s.acc_dk : &s.acc_dv;
-    uint64_t* other_acc = who == 0 ? &s.acc_dv : &s.acc_dk;
+    uint64_t* my_acc = who == 0 ? &s.acc_dv : &s.acc_dk;
+    uint64_t* my_sfull = who == 0 ? &s.s_full_s : &s.s_full_dp;
+    uint64_t* my_pfull = who == 0 ? &s.p_full_p : &s.p_full_ds;
     for (int gi = 0; ok && gi < n_groups; ++gi) {
       const int st = gi & 1;
       if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
-          (gi > 0 && !ptx::mbar_wait(other_acc, (gi - 1) & 1, abort))) { ok = false; break; }
+          (gi > 0 && !ptx::mbar_wait(my_acc, (gi - 1) & 1, abort))) { ok = false; break; }
       ptx::tc_fence_after_sync();
       if (lane == 0) {
         if (who == 0) mma_kk(tmem + kColS, ka, ptx::smem_u32(s.q[st]));
         else mma_kk(tmem + kColDP, va, ptx::smem_u32(s.dO[st]));
-        ptx::umma_commit(&s.s_full);
+        ptx::umma_commit(my_sfull);
       }
       issued_any = true;
       __syncwarp();
-      if (!ptx::mbar_wait(&s.p_full, gi & 1, abort)) { ok = false; break; }
+      if (!ptx::mbar_wait(my_pfull, gi & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       if (lane == 0) {
-        if (who == 0) mma_tmn(tmem + kColDK, tmem + kColDP, ptx::smem_u32(s.q[st]), gi > 0, true);
-        else mma_tmn(tmem + kColDV, tmem + kColS, ptx::smem_u32(s.dO[st]), gi > 0, true);
+        if (who == 0) mma_tmn(tmem + kColDV, tmem + kColS, ptx::smem_u32(s.dO[st]), gi > 0, true);
+        else mma_tmn(tmem + kColDK, tmem + kColDP, ptx::smem_u32(s.q[st]), gi > 0, true);
         ptx::umma_commit(my_acc);
         ptx::umma_commit(&s.g_empty[st]);
       }
@@ -595,48 +602,61 @@ backward_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int t0 = m * kQt + part * tok_per_group;
       const int dj = key - t0;
       const int xlim = dj > 0 ? dj * G : 0;
-      // g_full: the group's per-row lse2 / D have landed; s_full: S^T, dP^T
+      // g_full: the group's per-row lse2 / D have landed; then S^T
       if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
-          !ptx::mbar_wait(&s.s_full, gi & 1, abort)) { ok = false; break; }
+          !ptx::mbar_wait(&s.s_full_s, gi & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
-      uint32_t sv[1][32], dpv[1][32];
-#pragma unroll
-      for (int u = 0; u < 1; ++u) {
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + (half + u) * 32, sv[u]);
-        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (half + u) * 32, dpv[u]);
-      }
+      const int c = half;                                  // this warp's 32-column chunk
+      uint32_t sv[32];
+      ptx::tmem_ld_x32(tmem + lane_off + kColS + c * 32, sv);
       ptx::tmem_ld_wait();
-#pragma unroll
-      for (int u = 0; u < 1; ++u) {
-        const int c = half + u;
-        uint32_t pp[16], dd[16];
+      // P^T, two rows at a time in paired fp32 (the record holds -lse2 and -D), released
+      // to the dV product before dS^T is formed
+      float pr[32];
+      {
+        uint32_t pp[16];
         const uint64_t c1x2 = f32x2(c1, c1);
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          // two rows at a time in paired fp32; the record holds -lse2 and -D
           const int x = c * 32 + e;
           const uint64_t nl2 = *reinterpret_cast<const uint64_t*>(&s.rec[st][x]);
-          const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(&s.rec[st][kRows + x]);
           float y0, y1;
-          split_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[u][e]), __uint_as_float(sv[u][e + 1])),
+          split_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])),
                                 c1x2, nl2), y0, y1);
-          const float p0 = x >= xlim ? ex2(y0) : 0.f;
-          const float p1 = x + 1 >= xlim ? ex2(y1) : 0.f;
+          pr[e] = x >= xlim ? ex2(y0) : 0.f;
+          pr[e + 1] = x + 1 >= xlim ? ex2(y1) : 0.f;
+          pp[e >> 1] = pack_bf16x2(pr[e], pr[e + 1]);
+        }
+        // over columns this warp loaded: chunk c at columns 32c .. 32c+15
+        ptx::tmem_st_x16(tmem + lane_off + kColS + 32 * c, pp);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s.p_full_p);
+      }
+      // then dP^T and dS^T = P^T (dP^T - D)
+      if (!ptx::mbar_wait(&s.s_full_dp, gi & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      uint32_t dpv[32];
+      ptx::tmem_ld_x32(tmem + lane_off + kColDP + c * 32, dpv);
+      ptx::tmem_ld_wait();
+      {
+        uint32_t dd[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const uint64_t nd2 = *reinterpret_cast<const uint64_t*>(&s.rec[st][kRows + c * 32 + e]);
           float d0, d1;
-          split_f32x2(mul_f32x2(f32x2(p0, p1),
-                                add_f32x2(f32x2(__uint_as_float(dpv[u][e]), __uint_as_float(dpv[u][e + 1])), nd2)),
+          split_f32x2(mul_f32x2(f32x2(pr[e], pr[e + 1]),
+                                add_f32x2(f32x2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd2)),
                       d0, d1);
-          pp[e >> 1] = pack_bf16x2(p0, p1);
           dd[e >> 1] = pack_bf16x2(d0, d1);
         }
-        // P^T / dS^T over columns this warp loaded: chunk c at columns 32c .. 32c+15
-        ptx::tmem_st_x16(tmem + lane_off + kColS + 32 * c, pp);
         ptx::tmem_st_x16(tmem + lane_off + kColDP + 32 * c, dd);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&s.p_full_ds);
       }
-      ptx::tmem_st_wait();
-      ptx::tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&s.p_full);
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x603);
     bool have = ok && ptx::mbar_wait(&s.acc_dk, (n_groups - 1) & 1, abort) &&
