@@ -46,6 +46,7 @@ constexpr int kMaxSel = 256;
 constexpr int kMathWarps = 16;                          // four per TMEM lane quadrant
 constexpr int kProducerWarp = kMathWarps, kMmaWarp = kMathWarps + 1;   // MMA issuers: 17, 18
 constexpr int kThreads = (kMathWarps + 3) * 32;
+constexpr int kDqThreads = (kMathWarps + 4) * 32;     // dQ pass: three MMA issuers
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescKK = ptx::idesc_bf16_f32(128, 128, 0, 0);   // both operands K-major
 constexpr uint32_t kIdescMN = ptx::idesc_bf16_f32(128, 128, 0, 1);   // B MN-major
@@ -136,22 +137,29 @@ __global__ void selection_bitmap_kernel(const int32_t* __restrict__ sel,
 
 // ============================================================================ dQ kernel
 
+// dQ pass: K rides a three-stage ring (read by S and, a block later, by dQ), V a two-stage
+// ring (read by dP only, so free as soon as dP completes); with Q and dO this fills the
+// 227 KiB a CTA may use
+constexpr int kKStages = 3;
+
 struct __align__(1024) SmemQ {
   uint8_t q[kTileBytes];
   uint8_t dO[kTileBytes];
-  uint8_t k[2][kTileBytes];
+  uint8_t k[kKStages][kTileBytes];
   uint8_t v[2][kTileBytes];
   uint64_t qd_full;
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full, s_free, ds_full, dq_done, drain[2];
+  uint64_t k_full[kKStages], k_empty[kKStages], v_full[2], v_empty[2];
+  uint64_t s_full, s_free, ds_full, dq_done, drain[3];
   float dsum[kRows];
   int blocks[kMaxSel];
   int n_sel;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(SmemQ) + 1024 <= 227 * 1024, "dQ pass shared memory");
 
-__global__ void __launch_bounds__(kThreads, 1)
+
+__global__ void __launch_bounds__(kDqThreads, 1)
 backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_do,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -173,16 +181,19 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&s.qd_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(&s.kv_full[i], 1);
-      ptx::mbar_init(&s.kv_empty[i], 1);
+    for (int i = 0; i < kKStages; ++i) {
+      ptx::mbar_init(&s.k_full[i], 1);
+      ptx::mbar_init(&s.k_empty[i], 1);
     }
-    ptx::mbar_init(&s.s_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&s.v_full[i], 1);
+      ptx::mbar_init(&s.v_empty[i], 1);
+    }
+    ptx::mbar_init(&s.s_full, 2);          // S and dP, one commit each
     ptx::mbar_init(&s.s_free, kMathWarps);
     ptx::mbar_init(&s.ds_full, kMathWarps);
     ptx::mbar_init(&s.dq_done, 1);
-    ptx::mbar_init(&s.drain[0], 1);
-    ptx::mbar_init(&s.drain[1], 1);
+    for (int i = 0; i < 3; ++i) ptx::mbar_init(&s.drain[i], 1);
     s.abort = 0;
     ptx::fence_barrier_init();
   }
@@ -214,7 +225,7 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------- TMA producer
-    int issued = 0;
+    int issued_v = 0, issued_k = 0;
     bool ok = true;
     // test hook: issue nothing, so the consumers' bounded waits run out
     const int n_load = p.inject == 1 ? 0 : n_sel;
@@ -228,48 +239,62 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
     for (int j = 0; j < n_load; ++j) {
-      const int st = j & 1;
-      if (!ptx::mbar_wait(&s.kv_empty[st], ((j >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+      const int blk = s.blocks[j];
+      const int sv = j & 1, sk = j % kKStages;
+      if (!ptx::mbar_wait(&s.v_empty[sv], ((j >> 1) & 1) ^ 1, abort)) { ok = false; break; }
       if (lane == 0) {
-        const int blk = s.blocks[j];
-        ptx::mbar_arrive_expect_tx(&s.kv_full[st], 2 * kTileBytes);
-        for (int kc = 0; kc < 2; ++kc) {
-          ptx::tma_load_3d(s.k[st] + kc * kBk * kRowBytes, &tm_k, &s.kv_full[st], kc * 64,
+        ptx::mbar_arrive_expect_tx(&s.v_full[sv], kTileBytes);
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_3d(s.v[sv] + kc * kBk * kRowBytes, &tm_v, &s.v_full[sv], kc * 64,
                            blk * kBk, bg);
-          ptx::tma_load_3d(s.v[st] + kc * kBk * kRowBytes, &tm_v, &s.kv_full[st], kc * 64,
-                           blk * kBk, bg);
-        }
       }
-      issued = j + 1;
+      issued_v = j + 1;
+      __syncwarp();
+      if (!ptx::mbar_wait(&s.k_empty[sk], ((j / kKStages) & 1) ^ 1, abort)) { ok = false; break; }
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(&s.k_full[sk], kTileBytes);
+        for (int kc = 0; kc < 2; ++kc)
+          ptx::tma_load_3d(s.k[sk] + kc * kBk * kRowBytes, &tm_k, &s.k_full[sk], kc * 64,
+                           blk * kBk, bg);
+      }
+      issued_k = j + 1;
       __syncwarp();
     }
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x501);
     if (*abort && lane == 0 && n_load > 0) {
       ptx::mbar_wait_timed(&s.qd_full, 0);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        ptx::mbar_wait_timed(&s.kv_full[j & 1], (j >> 1) & 1);
+      for (int j = issued_v > 2 ? issued_v - 2 : 0; j < issued_v; ++j)
+        ptx::mbar_wait_timed(&s.v_full[j & 1], (j >> 1) & 1);
+      for (int j = issued_k > kKStages ? issued_k - kKStages : 0; j < issued_k; ++j)
+        ptx::mbar_wait_timed(&s.k_full[j % kKStages], (j / kKStages) & 1);
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+  } else if (warp >= kMmaWarp && warp <= kMmaWarp + 2) {
     // ------------------------------------------------------------- MMA issuers
-    // the first issuer: S = Q K^T and dP = dO V^T of each block (into TMEM once the math
-    // warps have read the previous block's); the second: dQ += dS K once the math warps
-    // have written dS.
-    // One thread's stream of N = 128 MMAs with commits keeps the tensor core busy only
-    // ~60 % of the time; two streams fill it.
+    // the first: S = Q K^T of each block, the second: dP = dO V^T (each into TMEM once the
+    // math warps have read the previous block's), the third: dQ += dS K once the math warps
+    // have written dS.  One thread's stream of N = 128 MMAs with commits runs at ~105 clocks
+    // an MMA, so S and dP (16 MMAs a block) on one thread held the block back; on two, the
+    // next block's S and dP run while this block's elementwise step forms dS.
     const int who = warp - kMmaWarp;
     bool ok = true, issued_any = false;
     const uint32_t qa = ptx::smem_u32(s.q), da = ptx::smem_u32(s.dO);
-    if (n_sel > 0 && who == 0) {
+    if (n_sel > 0 && who < 2) {
       ok = ptx::mbar_wait(&s.qd_full, 0, abort);
       for (int j = 0; ok && j < n_sel; ++j) {
-        // S / dP of block j once the math warps have read block j-1's
-        if (!ptx::mbar_wait(&s.kv_full[j & 1], (j >> 1) & 1, abort) ||
+        // S (first issuer) or dP (second) of block j once the math warps have read block j-1's
+        if ((who == 0 ? !ptx::mbar_wait(&s.k_full[j % kKStages], (j / kKStages) & 1, abort)
+                      : !ptx::mbar_wait(&s.v_full[j & 1], (j >> 1) & 1, abort)) ||
             (j > 0 && !ptx::mbar_wait(&s.s_free, (j - 1) & 1, abort))) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
-          mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[j & 1]));
-          mma_kk(tmem + kColDP, da, ptx::smem_u32(s.v[j & 1]));
-          ptx::umma_commit(&s.s_full);
+          if (who == 0) {
+            mma_kk(tmem + kColS, qa, ptx::smem_u32(s.k[j % kKStages]));
+            ptx::umma_commit(&s.s_full);
+          } else {
+            mma_kk(tmem + kColDP, da, ptx::smem_u32(s.v[j & 1]));
+            ptx::umma_commit(&s.s_full);
+            ptx::umma_commit(&s.v_empty[j & 1]);           // dP was the only reader of V
+          }
         }
         issued_any = true;
         __syncwarp();
@@ -279,11 +304,9 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
         if (!ptx::mbar_wait(&s.ds_full, j & 1, abort)) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
-          mma_tmn(tmem + kColDQ, tmem + kColDS, ptx::smem_u32(s.k[j & 1]), j > 0);
+          mma_tmn(tmem + kColDQ, tmem + kColDS, ptx::smem_u32(s.k[j % kKStages]), j > 0);
           ptx::umma_commit(&s.dq_done);
-          // block j's K and V are free: its S and dP completed before the math warps
-          // formed dS, and this dQ product was the last to read K
-          ptx::umma_commit(&s.kv_empty[j & 1]);
+          ptx::umma_commit(&s.k_empty[j % kKStages]);
         }
         issued_any = true;
         __syncwarp();
@@ -338,42 +361,42 @@ backward_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
     for (int j = 0; j < n_sel; ++j) {
       const int blk = s.blocks[j];
       if (!ptx::mbar_wait(&s.s_full, j & 1, abort)) { ok = false; break; }
-      // the previous block's dQ MMA has finished reading dS
-      if (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort)) { ok = false; break; }
       ptx::tc_fence_after_sync();
       const int lim = t - blk * kBk;                       // visible columns: c <= lim
-      uint32_t sv[1][32], dv[1][32];
-#pragma unroll
-      for (int u = 0; u < 1; ++u) {
-        ptx::tmem_ld_x32(tmem + lane_off + kColS + (half + u) * 32, sv[u]);
-        ptx::tmem_ld_x32(tmem + lane_off + kColDP + (half + u) * 32, dv[u]);
-      }
+      uint32_t sv[32], dv[32];
+      ptx::tmem_ld_x32(tmem + lane_off + kColS + half * 32, sv);
+      ptx::tmem_ld_x32(tmem + lane_off + kColDP + half * 32, dv);
       ptx::tmem_ld_wait();
       // this warp's S / dP columns are in registers: the next block may overwrite them
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s.s_free);
+      // The Q / dO barrier's only phase has completed, so this wait returns at once.  It is
+      // here because it is a loop: without it the compiler schedules the exponentials below
+      // ahead of the arrive, and the next block's S and dP wait for the whole elementwise
+      // step (measured: 2.9K instead of 2.3K clocks a block).
+      if (!ptx::mbar_wait(&s.qd_full, 0, abort)) { ok = false; break; }
+      uint32_t pk[16];
+      const uint64_t c1x2 = f32x2(c1, c1), nl2 = f32x2(-lse2, -lse2), nd2 = f32x2(-dsum, -dsum);
 #pragma unroll
-      for (int u = 0; u < 1; ++u) {
-        const int c = half + u;
-        uint32_t pk[16];
-        const uint64_t c1x2 = f32x2(c1, c1), nl2 = f32x2(-lse2, -lse2), nd2 = f32x2(-dsum, -dsum);
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          // two columns at a time in paired fp32
-          float y0, y1;
-          split_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[u][e]), __uint_as_float(sv[u][e + 1])),
-                                c1x2, nl2), y0, y1);
-          const float p0 = c * 32 + e <= lim ? ex2(y0) : 0.f;
-          const float p1 = c * 32 + e + 1 <= lim ? ex2(y1) : 0.f;
-          float d0, d1;
-          split_f32x2(mul_f32x2(f32x2(p0, p1),
-                                add_f32x2(f32x2(__uint_as_float(dv[u][e]), __uint_as_float(dv[u][e + 1])), nd2)),
-                      d0, d1);
-          pk[e >> 1] = pack_bf16x2(d0, d1);
-        }
-        ptx::tmem_st_x16(tmem + lane_off + kColDS + c * 16, pk);
+      for (int e = 0; e < 32; e += 2) {
+        // two columns at a time in paired fp32
+        float y0, y1;
+        split_f32x2(fma_f32x2(f32x2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c1x2,
+                              nl2), y0, y1);
+        const float p0 = half * 32 + e <= lim ? ex2(y0) : 0.f;
+        const float p1 = half * 32 + e + 1 <= lim ? ex2(y1) : 0.f;
+        float d0, d1;
+        split_f32x2(mul_f32x2(f32x2(p0, p1),
+                              add_f32x2(f32x2(__uint_as_float(dv[e]), __uint_as_float(dv[e + 1])),
+                                        nd2)),
+                    d0, d1);
+        pk[e >> 1] = pack_bf16x2(d0, d1);
       }
+      // the previous block's dQ MMA has finished reading dS (it ran while these were formed)
+      if (j > 0 && !ptx::mbar_wait(&s.dq_done, (j - 1) & 1, abort)) { ok = false; break; }
+      ptx::tc_fence_after_sync();
+      ptx::tmem_st_x16(tmem + lane_off + kColDS + half * 16, pk);
       ptx::tmem_st_wait();
       ptx::tc_fence_before_sync();
       __syncwarp();
@@ -770,7 +793,7 @@ cudaError_t launch_sparse_backward_tc(const Dims& p, const void* q, const void* 
                              (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(p.Qt * p.G / kRows, p.nR, p.B * p.Hkv);
-    backward_dq_tc_kernel<<<grid, kThreads, smem, st>>>(
+    backward_dq_tc_kernel<<<grid, kDqThreads, smem, st>>>(
         tq, tdo, tk, tv, sel, (const __nv_bfloat16*)out, (const __nv_bfloat16*)dout, lse, dq,
         rowstat, p, status);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
