@@ -453,6 +453,10 @@ kl_rows_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       ptx::tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&s.z_free2);
+      // The Q barrier's only phase has completed, so this wait returns at once; as a loop it
+      // keeps the compiler from scheduling the exponentials below ahead of the arrive, which
+      // would hold the next block's Z back for the whole elementwise step.
+      if (!ptx::mbar_wait(&s.q_full, 0, abort)) { ok = false; break; }
 #pragma unroll
       for (int u = 0; u < kCols32; ++u) {
         const int c = kCols32 * half + u;
