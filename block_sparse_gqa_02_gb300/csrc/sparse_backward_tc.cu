@@ -24,9 +24,11 @@
 //   vector atomics (a heavily selected block is split over several CTAs).
 // Warps: 16 elementwise warps (four per TMEM lane quadrant, each taking a quarter of the
 // columns of S / dP or S^T / dP^T: with two, the warps waited mostly on the latency of their
-// own loads and exponentials), a TMA producer and two MMA issuers (a single thread's stream
-// of N = 128 MMAs with commits in it keeps the tensor core busy only ~60 % of the time).
-// Every wait is bounded.
+// own loads and exponentials), a TMA producer and MMA issuers (a single thread's stream of
+// N = 128 MMAs with commits in it keeps the tensor core busy only ~60 % of the time): three
+// in the dQ kernel (S, dP, dQ), whose elementwise warps release S / dP as soon as they have
+// loaded them so the next block's products run while dS is formed; two in the dK / dV
+// kernel.  Every wait is bounded.
 #include "common.cuh"
 #include "ptx.cuh"
 #include "sparse_backward_tc.cuh"
@@ -44,7 +46,7 @@ constexpr int kRowBytes = 128;
 constexpr int kTileBytes = 2 * kRows * kRowBytes;       // [2 chunks][128 rows][128 B] = 32 KiB
 constexpr int kMaxSel = 256;
 constexpr int kMathWarps = 16;                          // four per TMEM lane quadrant
-constexpr int kProducerWarp = kMathWarps, kMmaWarp = kMathWarps + 1;   // MMA issuers: 17, 18
+constexpr int kProducerWarp = kMathWarps, kMmaWarp = kMathWarps + 1;   // first MMA issuer: 17
 constexpr int kThreads = (kMathWarps + 3) * 32;
 constexpr int kDqThreads = (kMathWarps + 4) * 32;     // dQ pass: three MMA issuers
 constexpr uint32_t kTmemCols = 512;
