@@ -808,20 +808,27 @@ kl_norm_tc_kernel(const __grid_constant__ CUtensorMap tm_ik, const __grid_consta
 constexpr int kIqRows = 64;                                   // idx_q rows of a group, padded
 constexpr int kIqBytes = 2 * kIqRows * kRowBytes;             // [2 chunks][64 rows][128 B]
 
+// A group's q, idx_q and record ride a three-stage ring: a stage is refilled only once the
+// group's d idx_k product has read its idx_q, so with two stages the next copies waited for
+// that product and the S^T / Z^T behind them, and the math warps for both.
+constexpr int kGStages = 3;
+
 struct __align__(1024) SmemK {
   uint8_t k[kTileBytes];
   uint8_t ik[kTileBytes];
-  uint8_t q[2][kTileBytes];
-  uint8_t iq[2][kIqBytes];
+  uint8_t q[kGStages][kTileBytes];
+  uint8_t iq[kGStages][kIqBytes];
   uint8_t gzs[2][2 * 16 * kRowBytes];   // gz (16 tokens x 128 keys, K-major) for d idx_q^T
-  float rec[2][2 * kRows];     // a group's -lse2 per row [0,128), -lseI2 per token [128,..)
-  uint64_t kv_full, g_full[2], g_empty[2];
+  float rec[kGStages][2 * kRows];   // a group's -lse2 per row [0,128), -lseI2 per token [128,..)
+  uint64_t kv_full, g_full[kGStages], g_empty[kGStages];
   uint64_t s_full[2], p_full[2], acc_done[2], drain[2];   // per S^T / gz^T buffer
-  int tiles[kMaxTilesPerCta];
+  uint16_t tiles[kMaxTilesPerCta];   // query tiles (< 65536) that selected the block
   int n_tiles;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(SmemK) + 1024 <= 227 * 1024, "key-block pass shared memory");
+
 
 // Warps of the key-block pass: 4 math warps per TMEM lane quadrant (each a quarter of a
 // group's rows) when a quarter holds whole packed gz^T columns (G <= 16), else 2.
@@ -866,7 +873,7 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane >= o) incl += y;
       }
       int pos = n + incl - cnt;
-      for (uint32_t x = word; x; x &= x - 1) s.tiles[pos++] = w * 32 + __ffs(x) - 1;
+      for (uint32_t x = word; x; x &= x - 1) s.tiles[pos++] = (uint16_t)(w * 32 + __ffs(x) - 1);
       n += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) s.n_tiles = n;
@@ -879,14 +886,14 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
   // the idx_q rows past a group's tokens stay zero (the copies write only kTok rows)
   using W = KeysWarps<G>;
-  for (int i = threadIdx.x; i < 2 * kIqBytes / 16; i += W::kThreads)
+  for (int i = threadIdx.x; i < kGStages * kIqBytes / 16; i += W::kThreads)
     reinterpret_cast<uint4*>(&s.iq[0][0])[i] = make_uint4(0, 0, 0, 0);
   // so do the gz rows past a group's tokens in the d idx_q^T operand
   for (int i = threadIdx.x; i < (int)sizeof(s.gzs) / 16; i += W::kThreads)
     reinterpret_cast<uint4*>(&s.gzs[0][0])[i] = make_uint4(0, 0, 0, 0);
   if (threadIdx.x == 0) {
     ptx::mbar_init(&s.kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kGStages; ++i) {
       ptx::mbar_init(&s.g_full[i], 1);
       ptx::mbar_init(&s.g_empty[i], 1);
     }
@@ -934,8 +941,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     }
     for (int gi = 0; gi < n_groups; ++gi) {
-      const int st = gi & 1;
-      if (!ptx::mbar_wait(&s.g_empty[st], ((gi >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+      const int st = gi % kGStages;
+      if (!ptx::mbar_wait(&s.g_empty[st], ((gi / kGStages) & 1) ^ 1, abort)) { ok = false; break; }
       const int m = s.tiles[gi / parts], part = gi % parts;
       const int t0 = m * kQt + part * kTok;
       if (lane == 0) {
@@ -955,8 +962,8 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (!ok && lane == 0) raise_abort(&s.abort, status, 0x711);
     if (*abort && lane == 0) {
       ptx::mbar_wait_timed(&s.kv_full, 0);
-      for (int gi = issued > 2 ? issued - 2 : 0; gi < issued; ++gi)
-        ptx::mbar_wait_timed(&s.g_full[gi & 1], (gi >> 1) & 1);
+      for (int gi = issued > kGStages ? issued - kGStages : 0; gi < issued; ++gi)
+        ptx::mbar_wait_timed(&s.g_full[gi % kGStages], (gi / kGStages) & 1);
     }
   } else if (warp == W::kMma || warp == W::kMma + 1) {
     // the first issuer: S^T and Z^T of each group (after the math warps released the
@@ -966,11 +973,11 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     bool issued_any = false;
     const uint32_t ka = ptx::smem_u32(s.k), ia = ptx::smem_u32(s.ik);
     for (int gi = 0; ok && gi < n_groups; ++gi) {
-      const int st = gi & 1, bf = gi % kNBuf;
+      const int st = gi % kGStages, bf = gi % kNBuf;
       const uint32_t ph = (gi / kNBuf) & 1;
       if (who == 0) {
         // S^T and Z^T of group gi, into a buffer the math warps have finished with
-        if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
+        if (!ptx::mbar_wait(&s.g_full[st], (gi / kGStages) & 1, abort) ||
             (gi >= kNBuf && !ptx::mbar_wait(&s.p_full[bf], ph ^ 1, abort))) { ok = false; break; }
         ptx::tc_fence_after_sync();
         if (lane == 0) {
@@ -1058,11 +1065,11 @@ kl_keys_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       }
     };
     for (int gi = 0; gi < n_groups; ++gi) {
-      const int st = gi & 1, bf = gi % kNBuf;
+      const int st = gi % kGStages, bf = gi % kNBuf;
       const uint32_t ph = (gi / kNBuf) & 1;
       const int m = s.tiles[gi / parts], part = gi % parts;
       const int t0 = m * kQt + part * kTok;
-      if (!ptx::mbar_wait(&s.g_full[st], (gi >> 1) & 1, abort) ||
+      if (!ptx::mbar_wait(&s.g_full[st], (gi / kGStages) & 1, abort) ||
           !ptx::mbar_wait(&s.s_full[bf], ph, abort) ||
           // the d idx_k MMA of the group that last used this gz^T buffer has read it
           (gi >= kNBuf && !ptx::mbar_wait(&s.acc_done[bf], ph ^ 1, abort))) { ok = false; break; }
@@ -1258,7 +1265,8 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
 
 bool index_kl_tc_supported(const Dims& p) {
   return p.dtype == 1 && !p.decode && p.d == kD && p.dI == kD && p.Bk == kBk && p.Qt == kQt &&
-         (p.G == 2 || p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32) && p.k <= kMaxSel;
+         (p.G == 2 || p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32) && p.k <= kMaxSel &&
+         p.nR <= 65536;                                   // tile indices held in 16 bits
 }
 
 size_t index_kl_tc_workspace_bytes(const Dims& p) {
