@@ -1253,6 +1253,8 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
     if (e != cudaSuccess) return e;
     const int words = (p.nR + 31) / 32;
     const int wpc = tiles_per_cta(p) / 32;
+    // a CTA lists at most wpc * 32 tiles in its shared tile list
+    if (wpc * 32 > kMaxTilesPerCta) return cudaErrorInvalidValue;
     dim3 grid((words + wpc - 1) / wpc, p.nB, p.B * p.Hkv);
     kern<<<grid, KeysWarps<G>::kThreads, smem, st>>>(tq, tk, tik, tiq, bits, rowstat, d_idx_k,
                                                      d_idx_q, loss, p, words, wpc, status);
