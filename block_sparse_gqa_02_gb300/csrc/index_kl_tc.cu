@@ -1268,7 +1268,7 @@ cudaError_t launch_kl_tc(const Dims& p, const CUtensorMap& tq, const CUtensorMap
 bool index_kl_tc_supported(const Dims& p) {
   return p.dtype == 1 && !p.decode && p.d == kD && p.dI == kD && p.Bk == kBk && p.Qt == kQt &&
          (p.G == 2 || p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32) && p.k <= kMaxSel &&
-         p.nR <= 65536;                                   // tile indices held in 16 bits
+         p.nR <= 65536;   // tile indices held in 16 bits (the shape check allows 65535)
 }
 
 size_t index_kl_tc_workspace_bytes(const Dims& p) {

@@ -147,6 +147,18 @@ def test_python_binding_raises(lib):
     assert ei.value.status == MSA_ERR_INVALID_ARG
 
 
+def test_index_kl_tensor_core_covers_the_longest_accepted_sequence(lib):
+    """The tensor-core index KL keeps a key block's query-tile list in 16-bit entries; the
+    shape check accepts at most 65535 query tiles a sequence, so the longest accepted prefill
+    still takes that path, and one tile more is refused before anything runs."""
+    t = 65535 * 64
+    longest = make_shape(1, t, t, 32, 4, 128, 128, 128, 16, 64, "bf16")
+    assert lib.msa_workspace_bytes(ctypes.byref(longest), 3) > 0
+    past = make_shape(1, t + 64, t + 64, 32, 4, 128, 128, 128, 16, 64, "bf16")
+    assert lib.msa_workspace_bytes(ctypes.byref(past), 3) == 0
+    assert b"query tiles" in lib.msa_last_error()
+
+
 def test_training_workspace_and_checks(lib):
     """The tensor-core backward and index KL need a workspace (sized by which = 2 / 3) and
     refuse a missing or short one; CUDA-core shapes need none."""
